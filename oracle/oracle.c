@@ -1,0 +1,373 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for the fused adaLN norm+modulate row
+ * kernels.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * bench's CPU-baseline leg load it; the product path never does.  It shares
+ * no code, header, table or helper with the CUDA library.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
+ * Contraction must stay off: every "rn(a op b)" below is meant as one IEEE
+ * binary32 operation rounded to nearest-even, never fused into an FMA.
+ *
+ * Sources (the pages are web reports on the sglang diffusion kernels):
+ *  - "SGLang diffusion fused-op package guide", section "Norm + scale/shift
+ *    (adaLN)": the canonical RMS fragment order (thread tx owns columns
+ *    8*TPR*b + 8*tx + v, v fastest then b, one ordered fadd chain per
+ *    thread, squares rounded separately), the butterfly fold over offsets
+ *    1,2,4,8,16 (= the adjacent-pair tree), the aten modulate chain that
+ *    rounds to bf16 after 1+scale, after the product and after +shift, and
+ *    the residual variant round(gate*update) then round(residual+that).
+ *  - "PR #33854 report" (ERNIE-Image), key source excerpt: pass 1 sum of
+ *    squares, the WPR==2 combination w0+w1, s/D + eps, pass 2
+ *    (bf16)(x*rstd*w), bf16(1+scale), bf16(y*that), store of prod+shift.
+ *  - "PR #34126 report" (FLUX.1), motivation section: LayerNorm with
+ *    no affine as per-element Welford and a count-weighted combine; the
+ *    guide's bit-exact kernel section adds "128-thread Welford, guarded
+ *    reciprocal, shfl.down fold order".
+ *  - "PR #37123 report" (Qwen-Image), implementation section 3: one
+ *    epilogue doing per-head warp-reduced RMSNorm with weight, interleaved
+ *    RoPE from an fp32 cos/sin cache for Q and K, a copy for V, written to
+ *    joint buffers in [text, image] order.
+ *
+ * Readings where the pages are silent or disagree (all listed in the design
+ * notes): the reciprocal square root is the defined IEEE pair
+ * rn(1/rn(sqrt(v))) instead of the pages' rsqrt.approx; s/D is an IEEE
+ * division; more than two warp sums combine by the adjacent-pair tree
+ * padded with +0; the LayerNorm Welford multiplies by rn(1/n); the combine's
+ * parenthesisation and the 4-warp order (W0+W2)+(W1+W3) are ours; the QK
+ * head norm uses 16 logical threads of one 8-element fragment each; the
+ * RoPE cache row is [cos_0..cos_63 | sin_0..sin_63].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef uint16_t bf16_bits;
+
+/* ---------------------------------------------------------------- bf16 */
+
+/* bf16 -> fp32 is exact: the 16 bits become the high half of the word. */
+static float widen(bf16_bits h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* fp32 -> bf16, round to nearest, ties to even, by integer arithmetic on
+ * the bit pattern.  Any NaN becomes the quiet NaN 0x7FC0 with its sign. */
+static bf16_bits narrow(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return (bf16_bits)(((u >> 16) & 0x8000u) | 0x7FC0u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (bf16_bits)(u >> 16);
+}
+
+/* bf(f): the fp32 value of the bf16 nearest to f. */
+static float bf(float f) { return widen(narrow(f)); }
+
+/* One IEEE binary32 operation each (contraction is off for this file). */
+static float rn_add(float a, float b) { return a + b; }
+static float rn_sub(float a, float b) { return a - b; }
+static float rn_mul(float a, float b) { return a * b; }
+static float rn_div(float a, float b) { return a / b; }
+
+/* The defined reciprocal square root: two correctly rounded operations. */
+static float defined_rsqrt(float v) { return rn_div(1.0f, sqrtf(v)); }
+
+/* ----------------------------------------------------------- modulate */
+
+/* y = bf(rn(bf(n * bf(rn(1 + scale))) + shift)); n is already bf16.  The
+ * product of two bf16 values is exact in fp32, so bf() rounds it once. */
+static bf16_bits modulate(float n, float scale, float shift)
+{
+    float one_plus = bf(rn_add(1.0f, scale));
+    float p = bf(rn_mul(n, one_plus));
+    return narrow(rn_add(p, shift));
+}
+
+/* ------------------------------------------------------------ RMSNorm */
+
+/* Canonical sum of squares of one row of D = 64*TPR values.
+ * Logical thread tx in [0,TPR) owns columns 8*TPR*b + 8*tx + v, b,v in
+ * [0,8), and sums rn(x*x) into one sequential chain with v fastest.  Each
+ * group of 32 consecutive threads (a warp) folds its partials by the
+ * adjacent-pair tree; the warp sums fold by the same tree, padded with +0
+ * up to a power of two (two warps: w0 + w1).  Threads past TPR in the last
+ * warp contribute +0. */
+static float rms_sum_of_squares(const float *x, int64_t D)
+{
+    int64_t tpr = D / 64;
+    int64_t nwarps = (tpr + 31) / 32;
+    int64_t npow = 1;
+    while (npow < nwarps)
+        npow *= 2;
+    float *wsum = (float *)calloc((size_t)npow, sizeof(float));
+    for (int64_t w = 0; w < nwarps; ++w) {
+        float lane[32];
+        for (int l = 0; l < 32; ++l) {
+            int64_t tx = 32 * w + l;
+            float acc = 0.0f;
+            if (tx < tpr)
+                for (int b = 0; b < 8; ++b)
+                    for (int v = 0; v < 8; ++v) {
+                        float xv = x[8 * tpr * b + 8 * tx + v];
+                        acc = rn_add(acc, rn_mul(xv, xv));
+                    }
+            lane[l] = acc;
+        }
+        for (int off = 1; off < 32; off *= 2)
+            for (int i = 0; i < 32; i += 2 * off)
+                lane[i] = rn_add(lane[i], lane[i + off]);
+        wsum[w] = lane[0];
+    }
+    for (int64_t off = 1; off < npow; off *= 2)
+        for (int64_t i = 0; i < npow; i += 2 * off)
+            wsum[i] = rn_add(wsum[i], wsum[i + off]);
+    float s = wsum[0];
+    free(wsum);
+    return s;
+}
+
+/* Normalise + modulate one row given its widened values. */
+static void rms_row(const float *xrow, const bf16_bits *w, const bf16_bits *scale,
+                    const bf16_bits *shift, bf16_bits *y, int64_t D, float eps,
+                    float *stats)
+{
+    float s = rms_sum_of_squares(xrow, D);
+    float mean_sq = rn_div(s, (float)D);
+    float rstd = defined_rsqrt(rn_add(mean_sq, eps));
+    for (int64_t j = 0; j < D; ++j) {
+        float t = rn_mul(xrow[j], rstd);
+        float n = w ? bf(rn_mul(t, widen(w[j]))) : bf(t);
+        y[j] = modulate(n, widen(scale[j]), widen(shift[j]));
+    }
+    if (stats) {
+        stats[0] = s;
+        stats[1] = rstd;
+    }
+}
+
+/* y = bf16(rms(x) (*w) * (1+scale) + shift) for x [B,T,D]; scale/shift
+ * rows of batch b start at b*vs.  stats (nullable): per row {s, rstd}.
+ * Requires D % 64 == 0 (the CUDA library further requires D % 2048 == 0). */
+void oracle_rms_modulate(const bf16_bits *x, const bf16_bits *weight,
+                         const bf16_bits *scale, const bf16_bits *shift, int64_t vs,
+                         bf16_bits *y, int64_t B, int64_t T, int64_t D, float eps,
+                         float *stats)
+{
+    float *xrow = (float *)malloc((size_t)D * sizeof(float));
+    for (int64_t r = 0; r < B * T; ++r) {
+        int64_t b = r / T;
+        for (int64_t j = 0; j < D; ++j)
+            xrow[j] = widen(x[r * D + j]);
+        rms_row(xrow, weight, scale + b * vs, shift + b * vs, y + r * D, D, eps,
+                stats ? stats + 2 * r : NULL);
+    }
+    free(xrow);
+}
+
+/* Gated residual: r' = bf(rn(r + bf(rn(gate*h)))), stored to r_out, then the
+ * RMS row above on r'.  r_out may equal r (each element is read first). */
+void oracle_gated_rms_modulate(const bf16_bits *r, const bf16_bits *h,
+                               const bf16_bits *gate, const bf16_bits *weight,
+                               const bf16_bits *scale, const bf16_bits *shift, int64_t vs,
+                               bf16_bits *r_out, bf16_bits *y, int64_t B, int64_t T,
+                               int64_t D, float eps, float *stats)
+{
+    float *xrow = (float *)malloc((size_t)D * sizeof(float));
+    for (int64_t row = 0; row < B * T; ++row) {
+        int64_t b = row / T;
+        for (int64_t j = 0; j < D; ++j) {
+            float gh = bf(rn_mul(widen(gate[b * vs + j]), widen(h[row * D + j])));
+            bf16_bits rp = narrow(rn_add(widen(r[row * D + j]), gh));
+            r_out[row * D + j] = rp;
+            xrow[j] = widen(rp);
+        }
+        rms_row(xrow, weight, scale + b * vs, shift + b * vs, y + row * D, D, eps,
+                stats ? stats + 2 * row : NULL);
+    }
+    free(xrow);
+}
+
+/* ---------------------------------------------------------- LayerNorm */
+
+typedef struct {
+    float n, mean, m2;
+} welford;
+
+/* Count-weighted combine of two partial states (Chan, Golub, LeVeque),
+ * A being the lower lane or warp.  An empty side returns the other. */
+static welford welford_combine(welford A, welford B)
+{
+    if (B.n == 0.0f)
+        return A;
+    if (A.n == 0.0f)
+        return B;
+    welford o;
+    o.n = rn_add(A.n, B.n);
+    float c = rn_div(B.n, o.n);
+    float delta = rn_sub(B.mean, A.mean);
+    o.mean = rn_add(A.mean, rn_mul(delta, c));
+    o.m2 = rn_add(rn_add(A.m2, B.m2), rn_mul(rn_mul(rn_mul(delta, delta), A.n), c));
+    return o;
+}
+
+/* 128 logical threads; thread t owns the 8-element fragments starting at
+ * column 8*(t + 128*k), k = 0,1,... while < D, visited in k order, v = 0..7
+ * inside.  Per element (Welford): n += 1; d = x - mean;
+ * mean += d*rn(1/n); m2 += d*(x - mean).  Each warp of 32 threads folds by
+ * the shfl.down order (offsets 16,8,4,2,1: lane i takes i (+) i+off); the
+ * four warp results fold the same way with offsets 2,1. */
+static welford ln_statistics(const float *x, int64_t D)
+{
+    welford lane[128];
+    for (int t = 0; t < 128; ++t) {
+        welford s = {0.0f, 0.0f, 0.0f};
+        for (int64_t base = 8 * (int64_t)t; base < D; base += 8 * 128)
+            for (int v = 0; v < 8; ++v) {
+                float xv = x[base + v];
+                s.n = rn_add(s.n, 1.0f);
+                float inv_n = rn_div(1.0f, s.n);
+                float d = rn_sub(xv, s.mean);
+                s.mean = rn_add(s.mean, rn_mul(d, inv_n));
+                float d2 = rn_sub(xv, s.mean);
+                s.m2 = rn_add(s.m2, rn_mul(d, d2));
+            }
+        lane[t] = s;
+    }
+    welford warp[4];
+    for (int w = 0; w < 4; ++w) {
+        welford *l = lane + 32 * w;
+        for (int off = 16; off >= 1; off /= 2)
+            for (int i = 0; i < off; ++i)
+                l[i] = welford_combine(l[i], l[i + off]);
+        warp[w] = l[0];
+    }
+    for (int off = 2; off >= 1; off /= 2)
+        for (int i = 0; i < off; ++i)
+            warp[i] = welford_combine(warp[i], warp[i + off]);
+    return warp[0];
+}
+
+/* y = bf16(LN(x) * (1+scale) + shift), LayerNorm without affine;
+ * n = bf(rn(rn(x - mean) * rstd)), rstd = rn(1/rn(sqrt(rn(rn(m2/D) + eps)))).
+ * stats (nullable): per row {mean, m2, rstd}.  Requires D % 8 == 0. */
+void oracle_ln_modulate(const bf16_bits *x, const bf16_bits *scale, const bf16_bits *shift,
+                        int64_t vs, bf16_bits *y, int64_t B, int64_t T, int64_t D, float eps,
+                        float *stats)
+{
+    float *xrow = (float *)malloc((size_t)D * sizeof(float));
+    for (int64_t r = 0; r < B * T; ++r) {
+        int64_t b = r / T;
+        for (int64_t j = 0; j < D; ++j)
+            xrow[j] = widen(x[r * D + j]);
+        welford st = ln_statistics(xrow, D);
+        float var = rn_div(st.m2, (float)D);
+        float rstd = defined_rsqrt(rn_add(var, eps));
+        for (int64_t j = 0; j < D; ++j) {
+            float n = bf(rn_mul(rn_sub(xrow[j], st.mean), rstd));
+            y[r * D + j] = modulate(n, widen(scale[b * vs + j]), widen(shift[b * vs + j]));
+        }
+        if (stats) {
+            stats[3 * r + 0] = st.mean;
+            stats[3 * r + 1] = st.m2;
+            stats[3 * r + 2] = rstd;
+        }
+    }
+    free(xrow);
+}
+
+/* ------------------------------------------------- QK norm + RoPE + V */
+
+/* RMS of one head of 128 values: 16 logical threads, thread l owns columns
+ * 8l..8l+7 as one chain; the 16 partials fold by the adjacent-pair tree. */
+static float head_rstd(const float *x, float eps)
+{
+    float lane[16];
+    for (int l = 0; l < 16; ++l) {
+        float acc = 0.0f;
+        for (int v = 0; v < 8; ++v)
+            acc = rn_add(acc, rn_mul(x[8 * l + v], x[8 * l + v]));
+        lane[l] = acc;
+    }
+    for (int off = 1; off < 16; off *= 2)
+        for (int i = 0; i < 16; i += 2 * off)
+            lane[i] = rn_add(lane[i], lane[i + off]);
+    return defined_rsqrt(rn_add(rn_div(lane[0], 128.0f), eps));
+}
+
+/* Normalise one head with weight w, then rotate pairs (2i, 2i+1) by the
+ * cos/sin of cache row rope ([cos_0..cos_63 | sin_0..sin_63], fp32). */
+static float qk_head(const bf16_bits *src, const bf16_bits *w, const float *rope,
+                     float eps, bf16_bits *dst)
+{
+    float x[128], n[128];
+    for (int j = 0; j < 128; ++j)
+        x[j] = widen(src[j]);
+    float rstd = head_rstd(x, eps);
+    for (int j = 0; j < 128; ++j)
+        n[j] = bf(rn_mul(rn_mul(x[j], rstd), widen(w[j])));
+    for (int i = 0; i < 64; ++i) {
+        float c = rope[i], s = rope[64 + i];
+        float a = n[2 * i], b = n[2 * i + 1];
+        dst[2 * i] = narrow(rn_sub(rn_mul(a, c), rn_mul(b, s)));
+        dst[2 * i + 1] = narrow(rn_add(rn_mul(a, s), rn_mul(b, c)));
+    }
+    return rstd;
+}
+
+static void qk_stream(const bf16_bits *q, const bf16_bits *k, const bf16_bits *v, int64_t T,
+                      int64_t stride, int64_t H, const bf16_bits *wq, const bf16_bits *wk,
+                      const float *rope, float eps, int64_t out_row0, bf16_bits *q_out,
+                      bf16_bits *k_out, bf16_bits *v_out, float *rstd_out)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t orow = out_row0 + t;
+        for (int64_t hd = 0; hd < H; ++hd) {
+            int64_t src = t * stride + hd * 128;
+            int64_t dst = (orow * H + hd) * 128;
+            float rq = qk_head(q + src, wq, rope + t * 128, eps, q_out + dst);
+            float rk = qk_head(k + src, wk, rope + t * 128, eps, k_out + dst);
+            memcpy(v_out + dst, v + src, 128 * sizeof(bf16_bits));
+            if (rstd_out) {
+                rstd_out[(orow * 2 + 0) * H + hd] = rq;
+                rstd_out[(orow * 2 + 1) * H + hd] = rk;
+            }
+        }
+    }
+}
+
+/* Q/K: per-head RMSNorm with weight then interleaved RoPE; V: copy.  Inputs
+ * are row-strided views (row stride in elements, heads contiguous at 128);
+ * outputs are [T_txt + T_img, H, 128], text rows first.  rstd_out
+ * (nullable): [T_txt + T_img, 2 (q,k), H]. */
+void oracle_qk_norm_rope_epilogue(const bf16_bits *q_txt, const bf16_bits *k_txt,
+                                  const bf16_bits *v_txt, int64_t T_txt, int64_t txt_stride,
+                                  const bf16_bits *q_img, const bf16_bits *k_img,
+                                  const bf16_bits *v_img, int64_t T_img, int64_t img_stride,
+                                  int64_t H, const bf16_bits *wq_txt, const bf16_bits *wk_txt,
+                                  const bf16_bits *wq_img, const bf16_bits *wk_img,
+                                  const float *rope_txt, const float *rope_img, float eps_txt,
+                                  float eps_img, bf16_bits *q_out, bf16_bits *k_out,
+                                  bf16_bits *v_out, float *rstd_out)
+{
+    qk_stream(q_txt, k_txt, v_txt, T_txt, txt_stride, H, wq_txt, wk_txt, rope_txt, eps_txt, 0,
+              q_out, k_out, v_out, rstd_out);
+    qk_stream(q_img, k_img, v_img, T_img, img_stride, H, wq_img, wk_img, rope_img, eps_img,
+              T_txt, q_out, k_out, v_out, rstd_out);
+}
+
+/* ------------------------------------------------------ exported helpers */
+
+/* The oracle's own fp32 -> bf16 rounding, exposed so that tests can pin it
+ * against an independent formulation. */
+void oracle_round_bf16(const float *in, bf16_bits *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = narrow(in[i]);
+}

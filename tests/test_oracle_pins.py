@@ -1,0 +1,489 @@
+"""Pins of the CPU oracle to facts other than itself.
+
+Each check below would fail under a plausible slip in the oracle: a wrong
+rounding rule, a dropped term, a swapped loop order, a transposed operand or
+a wrong pairing.  Sources: the closed forms of the adaLN norm+modulate target
+(constant row and scale = -1 give y = shift; a +-a row gives +-1/sqrt(1+eps/a^2)),
+the canonical order described in the "SGLang diffusion fused-op package
+guide" (section "Norm + scale/shift (adaLN)"), hand-worked sums under
+tests/golden/, and an fp64 brute force that must agree within 2 bf16 ULP
+(y) and 1e-6 relative (fp32 rstd).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from dit_adaln_norm_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+EPS = 1e-6
+
+
+# ------------------------------------------------------------------ helpers
+
+def widen(bits):
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32)
+
+
+def bits_of(values_f32):
+    return synth.to_bf16_bits(np.asarray(values_f32, np.float32))
+
+
+def bf16_of_f64(v):
+    """Round fp64 values to bf16 (through torch) and return them as fp64."""
+    t = torch.from_numpy(np.asarray(v, np.float64)).to(torch.bfloat16).to(torch.float64)
+    return t.numpy()
+
+
+def bf16_ulp(mag):
+    """Spacing of bf16 at magnitude |mag| (fp64), floored at the subnormal step."""
+    mag = np.abs(np.asarray(mag, np.float64))
+    _, e = np.frexp(np.where(mag > 0, mag, 1.0))
+    return np.ldexp(1.0, np.maximum(e - 8, -133)) * np.where(mag > 0, 1.0, 0.0) + \
+        np.where(mag > 0, 0.0, 2.0 ** -133)
+
+
+def vec(B, D, values):
+    return bits_of(np.broadcast_to(np.asarray(values, np.float32), (B, D)).copy())
+
+
+# ----------------------------------------------------- c-0: bf16 rounding
+
+def _reference_round(u32):
+    """Independent formulation: nearest of the two bf16 neighbours in fp64,
+    ties to the even bf16 pattern; values past the largest bf16 round to inf
+    as if it were 2^128; NaN -> quiet NaN with its sign."""
+    u32 = np.asarray(u32, np.uint32)
+    lo = (u32 >> 16).astype(np.uint32)
+    hi = lo + 1
+    hi_is_inf = (hi & 0x7FFF) == 0x7F80
+    with np.errstate(over="ignore", invalid="ignore"):
+        f64 = u32.view(np.float32).astype(np.float64)
+        lo_val = (lo << 16).view(np.float32).astype(np.float64)
+        hi_val = np.where(hi_is_inf, np.copysign(2.0 ** 128, f64),
+                          (hi << 16).astype(np.uint32).view(np.float32).astype(np.float64))
+        d_lo = np.abs(f64 - lo_val)
+        d_hi = np.abs(hi_val - f64)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (lo & 1 == 1))
+    exact = (u32 & 0xFFFF) == 0
+    out = np.where(pick_hi & ~exact, hi, lo).astype(np.uint16)
+    nan = (u32 & 0x7FFFFFFF) > 0x7F800000
+    return np.where(nan, ((u32 >> 16) & 0x8000) | 0x7FC0, out).astype(np.uint16)
+
+
+def test_round_bf16_every_high_half_and_ties(orc):
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = np.array([0x0000, 0x0001, 0x7FFF, 0x8000, 0x8001, 0xFFFF], np.uint32)
+    u = (hi[:, None] | lows[None, :]).ravel()
+    got = orc.round_bf16(u.view(np.float32))
+    assert np.array_equal(got, _reference_round(u))
+
+
+def test_round_bf16_random_words(orc):
+    u = np.random.Generator(np.random.PCG64(7)).integers(0, 1 << 32, 2_000_000,
+                                                          dtype=np.uint64).astype(np.uint32)
+    assert np.array_equal(orc.round_bf16(u.view(np.float32)), _reference_round(u))
+
+
+def test_round_bf16_matches_torch_cast_on_finite(orc):
+    """torch's fp32 -> bf16 cast is a second, independent RNE implementation."""
+    u = np.random.Generator(np.random.PCG64(8)).integers(0, 1 << 32, 500_000,
+                                                          dtype=np.uint64).astype(np.uint32)
+    f = u.view(np.float32)
+    f = f[np.isfinite(f)]
+    assert np.array_equal(orc.round_bf16(f), synth.to_bf16_bits(f))
+
+
+# ---------------------------------------------- c-1: canonical RMS order
+
+def _probe_row(p):
+    D = p["D"]
+    x = np.zeros(D, np.float32)
+    cols = p["columns"]
+    if "ones_thread" in cols:
+        tpr = D // 64
+        tx = cols["ones_thread"]
+        for b in range(8):
+            for v in range(8):
+                x[8 * tpr * b + 8 * tx + v] = 1.0
+    for c, val in cols["big"]:
+        x[c] = val
+    return x
+
+
+@pytest.mark.parametrize("name", ["chain_v_fastest", "adjacent_pair_tree",
+                                  "three_warps_padded_tree", "four_warps_tree"])
+def test_rms_order_probes(orc, name):
+    probes = {p["name"]: p for p in json.load(open(os.path.join(GOLDEN,
+                                                                "rms_order_probes.json")))["probes"]}
+    p = probes[name]
+    D = p["D"]
+    x = bits_of(_probe_row(p))[None, None, :]
+    zeros = vec(1, D, 0.0)
+    _, st = orc.rms_modulate(x, zeros, zeros, EPS, with_stats=True)
+    assert st[0, 0] == np.float32(p["expected_s"]), (st[0, 0], p["expected_s"])
+
+
+@pytest.mark.parametrize("D", [2048, 4096, 6144, 8192])
+def test_rms_unit_magnitude_row(orc, D):
+    """All +-1 (random signs): s = D exactly; with scale = shift = 0 and
+    eps = 1e-6, y = +-1 exactly (1/sqrt(1 + 1e-6) rounds to 1 in bf16)."""
+    sgn = np.where(np.random.Generator(np.random.PCG64(D)).random((3, D)) < 0.5, -1.0, 1.0)
+    x = bits_of(sgn)[None]
+    zeros = vec(1, D, 0.0)
+    y, st = orc.rms_modulate(x, zeros, zeros, EPS, with_stats=True)
+    assert np.all(st[:, 0] == D)
+    assert np.array_equal(widen(y[0]), sgn.astype(np.float32))
+
+
+@pytest.mark.parametrize("a", [0.5, 1.5, 3.0, 96.0])
+def test_rms_alternating_closed_form(orc, a):
+    D = 4096
+    x = bits_of(a * (-1.0) ** np.arange(D))[None, None]
+    zeros = vec(1, D, 0.0)
+    y = orc.rms_modulate(x, zeros, zeros, EPS)
+    expect = (-1.0) ** np.arange(D) / np.sqrt(1.0 + EPS / a ** 2)
+    assert np.all(np.abs(widen(y[0, 0]) - expect) <= bf16_ulp(expect))
+
+
+def test_scale_minus_one_gives_shift(orc):
+    """o = bf(1 + (-1)) = 0, p = +-0, y = shift (as a value) for every variant."""
+    B, T, D = 2, 5, 4096
+    x = synth.normal_bf16((B, T, D), 3)
+    shift = synth.normal_bf16((B, D), 4, 0.5)
+    scale = vec(B, D, -1.0)
+    for y in (orc.rms_modulate(x, scale, shift, EPS), orc.ln_modulate(x, scale, shift, EPS),
+              orc.gated_rms_modulate(x, synth.normal_bf16((B, T, D), 5),
+                                     synth.normal_bf16((B, D), 6, 0.1), scale, shift, EPS)[1]):
+        assert np.array_equal(widen(y), np.broadcast_to(widen(shift)[:, None, :], (B, T, D)))
+
+
+def test_zero_row_gives_shift(orc):
+    B, T, D = 1, 2, 2048
+    x = np.zeros((B, T, D), np.uint16)
+    scale = synth.normal_bf16((B, D), 8, 0.3)
+    shift = synth.normal_bf16((B, D), 9, 0.3)
+    for y in (orc.rms_modulate(x, scale, shift, EPS), orc.ln_modulate(x, scale, shift, EPS)):
+        assert np.array_equal(widen(y), np.broadcast_to(widen(shift)[:, None, :], (B, T, D)))
+
+
+def test_rms_weight_one_and_two(orc):
+    B, T, D = 1, 4, 4096
+    x = synth.normal_bf16((B, T, D), 10)
+    zeros = vec(B, D, 0.0)
+    y0 = orc.rms_modulate(x, zeros, zeros, EPS)
+    y1 = orc.rms_modulate(x, zeros, zeros, EPS, weight=bits_of(np.ones(D)))
+    y2 = orc.rms_modulate(x, zeros, zeros, EPS, weight=bits_of(np.full(D, 2.0)))
+    assert np.array_equal(y0, y1)
+    assert np.array_equal(widen(y2), 2.0 * widen(y0))
+
+
+def test_sign_flip_and_power_of_two_scaling(orc):
+    """x -> -x negates n exactly; x -> 4x with eps = 0 leaves n unchanged
+    (every operation scales exactly by a power of two)."""
+    B, T, D = 1, 6, 3072
+    x = synth.outlier_rows_bf16((B, T, D), 11, 12)
+    zeros = vec(B, D, 0.0)
+    neg = x ^ np.uint16(0x8000)
+    x4 = bits_of(4.0 * widen(x))
+    for fn, Dk in ((orc.ln_modulate, D), (orc.rms_modulate, 3072)):
+        y = fn(x, zeros, zeros, EPS)
+        assert np.array_equal(widen(fn(neg, zeros, zeros, EPS)), -widen(y))
+        assert np.array_equal(fn(x4, zeros, zeros, 0.0), fn(x, zeros, zeros, 0.0))
+
+
+# ------------------------------------------------- c-2: LayerNorm Welford
+
+def test_ln_constant_rows(orc):
+    B, T, D = 2, 7, 3072
+    c = widen(synth.normal_bf16((B, T), 13, 3.0))
+    x = bits_of(np.broadcast_to(c[..., None], (B, T, D)))
+    scale = synth.normal_bf16((B, D), 14, 0.2)
+    shift = synth.normal_bf16((B, D), 15, 0.2)
+    y, st = orc.ln_modulate(x, scale, shift, EPS, with_stats=True)
+    assert np.array_equal(st[:, 0], c.ravel()) and np.all(st[:, 1] == 0)
+    assert np.array_equal(widen(y), np.broadcast_to(widen(shift)[:, None, :], (B, T, D)))
+
+
+def test_ln_two_chain_combine_by_hand(orc):
+    """D = 16: thread 0 holds eight 1s, thread 1 eight 3s.  Combine: n = 16,
+    c = 8/16, delta = 2, mean = 1 + 2*0.5 = 2, m2 = 0 + 0 + (4*8)*0.5 = 16;
+    var = 1, rstd = 1 (eps = 0), n = x - 2 = -+1."""
+    x = bits_of(np.r_[np.ones(8), np.full(8, 3.0)])[None, None]
+    zeros = vec(1, 16, 0.0)
+    y, st = orc.ln_modulate(x, zeros, zeros, 0.0, with_stats=True)
+    assert (st[0, 0], st[0, 1], st[0, 2]) == (2.0, 16.0, 1.0)
+    assert np.array_equal(widen(y[0, 0]), np.r_[-np.ones(8), np.ones(8)].astype(np.float32))
+
+
+def test_ln_three_chain_count_weights_by_hand(orc):
+    """D = 24: threads 0,1,2 hold eight 1s, 5s, 3s.  shfl.down order pairs
+    (t0 + t2) first: n 16, mean 2, m2 (2*2*8)*0.5 = 16; then + t1 (n 8,
+    mean 5): c = rn(8/24), delta = 3, mean = 2 + rn(3*c) = 3 and
+    m2 = 16 + rn(rn(9*16)*c) = 64, all exact after rounding.  Weighting by
+    nA/n instead of nB/n would give mean 4."""
+    x = bits_of(np.r_[np.ones(8), np.full(8, 5.0), np.full(8, 3.0)])[None, None]
+    zeros = vec(1, 24, 0.0)
+    _, st = orc.ln_modulate(x, zeros, zeros, 0.0, with_stats=True)
+    assert (st[0, 0], st[0, 1]) == (3.0, 64.0)
+
+
+@pytest.mark.parametrize("a", [1.0, 0.25, 3.0])
+def test_ln_alternating_closed_form(orc, a):
+    """+-a alternating row: mean 0, var a^2, y = +-1/sqrt(1 + eps/a^2)
+    within 2 bf16 ULP (Welford rounds from n = 3 on)."""
+    D = 3072
+    sgn = (-1.0) ** np.arange(D)
+    x = bits_of(a * sgn)[None, None]
+    zeros = vec(1, D, 0.0)
+    y = orc.ln_modulate(x, zeros, zeros, EPS)
+    expect = sgn / np.sqrt(1.0 + EPS / a ** 2)
+    assert np.all(np.abs(widen(y[0, 0]) - expect) <= 2 * bf16_ulp(expect))
+
+
+# ----------------------------------------------------- c-6: fp64 brute force
+
+def _check_modulated(y, n64, scale, shift):
+    """y (oracle bits) against the fp64 normalised value n64 carried through
+    the bf16 modulate boundaries: within 2 bf16 ULP of max(|p|, |shift|)."""
+    o = widen(bits_of(1.0 + widen(scale).astype(np.float32))).astype(np.float64)
+    p = bf16_of_f64(bf16_of_f64(n64) * o)
+    sh = widen(shift).astype(np.float64)
+    y64 = bf16_of_f64(p + sh)
+    tol = 2 * bf16_ulp(np.maximum(np.abs(p), np.abs(sh)))
+    err = np.abs(widen(y).astype(np.float64) - y64)
+    assert np.all(err <= tol), float((err / tol).max())
+
+
+@pytest.mark.parametrize("D", [64, 128, 256, 2048, 4096])
+def test_rms_fp64_brute_force(orc, D):
+    B, T = 2, 24
+    x = synth.normal_bf16((B, T, D), 20 + D)
+    scale, shift = synth.adaln_vectors(B, D, 2, 21, 0.1)
+    y, st = orc.rms_modulate(x, scale, shift, EPS, with_stats=True)
+    xf = widen(x).astype(np.float64)
+    s64 = (xf ** 2).sum(-1)
+    rstd64 = 1.0 / np.sqrt(s64 / D + EPS)
+    assert np.all(np.abs(st[:, 1] / rstd64.ravel() - 1.0) <= 1e-6)
+    assert np.all(np.abs(st[:, 0] / s64.ravel() - 1.0) <= 1e-5)
+    _check_modulated(y, xf * rstd64[..., None], scale[:, None, :], shift[:, None, :])
+
+
+def test_gated_fp64_brute_force(orc):
+    B, T, D = 1, 16, 4096
+    r = synth.normal_bf16((B, T, D), 30)
+    h = synth.normal_bf16((B, T, D), 31)
+    gate, scale, shift = synth.adaln_vectors(B, D, 3, 32, 0.1)
+    r_out, y = orc.gated_rms_modulate(r, h, gate, scale, shift, EPS)
+    exact = widen(r).astype(np.float64) + widen(gate)[:, None, :].astype(np.float64) * \
+        widen(h).astype(np.float64)
+    gh = np.abs(widen(gate)[:, None, :].astype(np.float64) * widen(h))
+    mag = np.maximum(np.maximum(np.abs(widen(r)), gh), np.abs(widen(r_out)))
+    assert np.all(np.abs(widen(r_out) - exact) <= bf16_ulp(mag))
+    # y is the RMS+modulate of r' (same oracle, consistency)...
+    assert np.array_equal(y, orc.rms_modulate(r_out, scale, shift, EPS))
+    # ...and within tolerance of the fp64 chain on r'.
+    rf = widen(r_out).astype(np.float64)
+    rstd64 = 1.0 / np.sqrt((rf ** 2).mean(-1) + EPS)
+    _check_modulated(y, rf * rstd64[..., None], scale[:, None, :], shift[:, None, :])
+
+
+def test_gated_special_gates(orc):
+    """gate = 0 -> r' = r; gate = 1 -> r' = bf16 of the exact r + h."""
+    B, T, D = 1, 3, 2048
+    r = synth.normal_bf16((B, T, D), 33)
+    h = synth.normal_bf16((B, T, D), 34)
+    zeros = vec(B, D, 0.0)
+    r0, _ = orc.gated_rms_modulate(r, h, zeros, zeros, zeros, EPS)
+    assert np.array_equal(widen(r0), widen(r))
+    r1, _ = orc.gated_rms_modulate(r, h, vec(B, D, 1.0), zeros, zeros, EPS)
+    exact = widen(r).astype(np.float64) + widen(h).astype(np.float64)
+    assert np.array_equal(widen(r1), bf16_of_f64(exact).astype(np.float32))
+
+
+@pytest.mark.parametrize("D,outliers", [(8, False), (64, False), (1040, False),
+                                        (3072, True), (4096, False), (4096, True)])
+def test_ln_fp64_brute_force(orc, D, outliers):
+    B, T = 2, 24
+    x = (synth.outlier_rows_bf16((B, T, D), 40 + D, 2) if outliers
+         else synth.normal_bf16((B, T, D), 40 + D))
+    scale, shift = synth.adaln_vectors(B, D, 2, 41, 0.2)
+    y, st = orc.ln_modulate(x, scale, shift, EPS, with_stats=True)
+    xf = widen(x).astype(np.float64)
+    mean64 = xf.mean(-1)
+    var64 = ((xf - mean64[..., None]) ** 2).mean(-1)
+    rstd64 = 1.0 / np.sqrt(var64 + EPS)
+    assert np.all(np.abs(st[:, 2] / rstd64.ravel() - 1.0) <= 1e-6)
+    assert np.all(np.abs(st[:, 0] - mean64.ravel()) <= 1e-6 * np.sqrt(var64.ravel()))
+    _check_modulated(y, (xf - mean64[..., None]) * rstd64[..., None],
+                     scale[:, None, :], shift[:, None, :])
+
+
+def test_batch_stride_and_batching_consistency(orc):
+    """A [B, D] strided view gives each batch's rows its own vectors: the same
+    as running every batch alone with contiguous vectors."""
+    B, T, D = 3, 5, 4096
+    x = synth.normal_bf16((B, T, D), 50)
+    scale, shift = synth.adaln_vectors(B, D, 2, 51, 0.2, chunks=6)
+    assert scale.strides[0] == 6 * D * 2
+    for fn in (orc.rms_modulate, orc.ln_modulate):
+        y = fn(x, scale, shift, EPS)
+        for b in range(B):
+            yb = fn(x[b:b + 1], np.ascontiguousarray(scale[b:b + 1]),
+                    np.ascontiguousarray(shift[b:b + 1]), EPS)
+            assert np.array_equal(y[b:b + 1], yb)
+
+
+# -------------------------------------------- c-5: QK norm + RoPE epilogue
+
+def _qk_inputs(Tt, Ti, H, seed):
+    pt = synth.packed_qkv(Tt, H, seed)
+    pi = synth.packed_qkv(Ti, H, seed + 1)
+    ws = synth.head_weights(4, seed + 2)
+    return pt, pi, ws
+
+
+def _rope_const(T, c, s):
+    return np.concatenate([np.full((T, 64), c, np.float32), np.full((T, 64), s, np.float32)], 1)
+
+
+def test_qk_identity_and_quarter_turn(orc):
+    """cos = 1, sin = 0 leaves the normalised head unchanged; cos = 0,
+    sin = 1 maps the interleaved pair (a, b) to (-b, a) exactly."""
+    Tt, Ti, H = 3, 5, 4
+    pt, pi, ws = _qk_inputs(Tt, Ti, H, 60)
+    txt, img = synth.split_qkv(pt, H), synth.split_qkv(pi, H)
+    q1, k1, v1 = orc.qk_norm_rope_epilogue(txt, img, H, ws, _rope_const(Tt, 1, 0),
+                                           _rope_const(Ti, 1, 0), EPS, EPS)
+    q2, k2, v2 = orc.qk_norm_rope_epilogue(txt, img, H, ws, _rope_const(Tt, 0, 1),
+                                           _rope_const(Ti, 0, 1), EPS, EPS)
+    for n, r in ((q1, q2), (k1, k2)):
+        nf, rf = widen(n), widen(r)
+        assert np.array_equal(rf[..., 0::2], -nf[..., 1::2])
+        assert np.array_equal(rf[..., 1::2], nf[..., 0::2])
+    assert np.array_equal(v1, v2)
+
+
+def test_qk_unit_head_closed_form(orc):
+    """A head of +-1 with weight 1 and cos = 1, sin = 0 comes out as +-1."""
+    Tt, Ti, H = 2, 2, 3
+    sgn = np.where(np.random.Generator(np.random.PCG64(61)).random((Tt + Ti, 3 * H * 128)) < 0.5,
+                   -1.0, 1.0)
+    packed = bits_of(sgn)
+    ones = [bits_of(np.ones(128))] * 4
+    q, k, v = orc.qk_norm_rope_epilogue(synth.split_qkv(packed[:Tt], H),
+                                        synth.split_qkv(packed[Tt:], H), H, ones,
+                                        _rope_const(Tt, 1, 0), _rope_const(Ti, 1, 0), EPS, EPS)
+    W = H * 128
+    assert np.array_equal(widen(q).reshape(-1, W), sgn[:, :W].astype(np.float32))
+    assert np.array_equal(widen(k).reshape(-1, W), sgn[:, W:2 * W].astype(np.float32))
+
+
+def test_qk_v_copy_and_joint_order(orc):
+    Tt, Ti, H = 4, 6, 2
+    pt, pi, ws = _qk_inputs(Tt, Ti, H, 62)
+    txt, img = synth.split_qkv(pt, H), synth.split_qkv(pi, H)
+    _, _, v = orc.qk_norm_rope_epilogue(txt, img, H, ws, synth.rope_table(Tt),
+                                        synth.rope_table(Ti), EPS, EPS)
+    assert np.array_equal(v[:Tt].reshape(Tt, -1), txt[2])
+    assert np.array_equal(v[Tt:].reshape(Ti, -1), img[2])
+
+
+def test_qk_fp64_brute_force(orc):
+    Tt, Ti, H = 8, 24, 3
+    pt, pi, ws = _qk_inputs(Tt, Ti, H, 63)
+    txt, img = synth.split_qkv(pt, H), synth.split_qkv(pi, H)
+    rt, ri = synth.rope_table(Tt), synth.rope_table(Ti, pos0=17)
+    eps_t, eps_i = 1e-6, 1e-5
+    q, k, v, rs = orc.qk_norm_rope_epilogue(txt, img, H, ws, rt, ri, eps_t, eps_i,
+                                            with_stats=True)
+    for s, (src, rope, eps, wq, wk, row0) in enumerate(
+            ((txt, rt, eps_t, ws[0], ws[1], 0), (img, ri, eps_i, ws[2], ws[3], Tt))):
+        T = src[0].shape[0]
+        for which, (x, w, out) in enumerate(((src[0], wq, q), (src[1], wk, k))):
+            xf = widen(x).astype(np.float64).reshape(T, H, 128)
+            rstd64 = 1.0 / np.sqrt((xf ** 2).mean(-1) + eps)
+            got_rstd = rs[row0:row0 + T, which, :]
+            assert np.all(np.abs(got_rstd / rstd64 - 1.0) <= 1e-6)
+            n = bf16_of_f64(xf * rstd64[..., None] * widen(w).astype(np.float64))
+            a, b = n[..., 0::2], n[..., 1::2]
+            c = rope[:, None, :64].astype(np.float64)
+            sn = rope[:, None, 64:].astype(np.float64)
+            e0, e1 = a * c - b * sn, a * sn + b * c
+            tol = 2 * bf16_ulp(np.maximum(np.abs(a), np.abs(b)))
+            o = widen(out[row0:row0 + T]).astype(np.float64)
+            assert np.all(np.abs(o[..., 0::2] - e0) <= tol)
+            assert np.all(np.abs(o[..., 1::2] - e1) <= tol)
+
+
+# ------------------------------------- hand-worked probes under tests/golden
+
+def _golden(name):
+    return {p["name"]: p for p in json.load(open(os.path.join(GOLDEN, name)))["probes"]}
+
+
+def _runs(runs):
+    return np.concatenate([np.full(n, v, np.float64) for v, n in runs])
+
+
+@pytest.mark.parametrize("name", ["welford_reciprocal", "lane_tree_down_order", "cross_warp_order"])
+def test_ln_order_probes(orc, name):
+    p = _golden("ln_order_probes.json")[name]
+    xs = np.asarray(p["x"], np.float64) if "x" in p else _runs(p["x_runs"])
+    D = p["D"]
+    assert xs.size == D
+    zeros = vec(1, D, 0.0)
+    _, st = orc.ln_modulate(bits_of(xs)[None, None], zeros, zeros, p["eps"], with_stats=True)
+    assert st[0, 0] == np.float32(p["expected_mean"]), (float(st[0, 0]), p["expected_mean"])
+    if "expected_m2" in p:
+        assert st[0, 1] == np.float32(p["expected_m2"]), (float(st[0, 1]), p["expected_m2"])
+
+
+def test_one_plus_scale_tie_probe(orc):
+    B, T, D = 1, 4, 4096
+    x = synth.normal_bf16((B, T, D), 70)
+    shift = synth.normal_bf16((B, D), 71, 0.2)
+    for fn in (orc.rms_modulate, orc.ln_modulate):
+        assert np.array_equal(fn(x, vec(B, D, 2.0 ** -8), shift, EPS),
+                              fn(x, vec(B, D, 0.0), shift, EPS))
+        assert np.array_equal(fn(x, vec(B, D, 3 * 2.0 ** -8), shift, EPS),
+                              fn(x, vec(B, D, 2.0 ** -6), shift, EPS))
+
+
+def test_rms_product_probe(orc):
+    p = _golden("rounding_boundary_probes.json")["rms_product_rounded_before_shift"]
+    D = p["D"]
+    y = orc.rms_modulate(bits_of(np.full((1, 1, D), p["x"])), vec(1, D, p["scale"]),
+                         vec(1, D, p["shift"]), p["eps"], weight=bits_of(np.full(D, p["weight"])))
+    assert np.all(widen(y) == np.float32(p["expected_y"]))
+
+
+def test_ln_product_probe(orc):
+    p = _golden("rounding_boundary_probes.json")["ln_product_rounded_before_shift"]
+    D = p["D"]
+    y = orc.ln_modulate(bits_of(_runs(p["x_runs"]))[None, None], vec(1, D, p["scale"]),
+                        vec(1, D, p["shift"]), p["eps"])
+    expect = _runs([(v, n) for v, (_, n) in zip(p["expected_y_runs"], p["x_runs"])])
+    assert np.array_equal(widen(y[0, 0]), expect.astype(np.float32))
+
+
+def test_gated_product_probe(orc):
+    p = _golden("rounding_boundary_probes.json")["gated_product_rounded_before_add"]
+    D = p["D"]
+    r_out, _ = orc.gated_rms_modulate(bits_of(np.full((1, 1, D), p["r"])),
+                                      bits_of(np.full((1, 1, D), p["h"])), vec(1, D, p["gate"]),
+                                      vec(1, D, 0.0), vec(1, D, 0.0), EPS)
+    assert np.all(widen(r_out) == np.float32(p["expected_r_out"]))
+
+
+def test_weight_single_rounding_probe(orc):
+    p = _golden("rounding_boundary_probes.json")["weight_single_rounding"]
+    D = p["D"]
+    x = np.tile(np.asarray(p["x_alternating"], np.float64), D // 2)
+    y = orc.rms_modulate(bits_of(x)[None, None], vec(1, D, p["scale"]), vec(1, D, p["shift"]),
+                         p["eps"], weight=bits_of(np.full(D, p["weight"])))
+    expect = np.tile(np.asarray(p["expected_y_alternating"], np.float32), D // 2)
+    assert np.array_equal(widen(y[0, 0]), expect)
