@@ -1,0 +1,44 @@
+// dan_internal.h -- launch interface between the C-ABI shim and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dan {
+
+// One row problem: [B, T, D] rows, per-batch vectors with batch stride vs
+// (elements), optional weight [D].  Arguments are validated by the shim.
+struct RowProblem {
+    const void *x;      // input rows (r for the gated form)
+    const void *h;      // gated update rows, or nullptr
+    const void *gate;   // per-batch gate, or nullptr
+    const void *weight; // [D] or nullptr
+    const void *scale;
+    const void *shift;
+    int64_t vs;
+    void *y;
+    void *r_out; // gated residual output, or nullptr
+    int64_t B, T, D;
+    float eps;
+};
+
+struct QkProblem {
+    const void *q[2], *k[2], *v[2]; // [0] text, [1] image
+    int64_t T[2];
+    int64_t stride[2]; // row stride in elements
+    const void *wq[2], *wk[2];
+    const float *rope[2];
+    float eps[2];
+    void *q_out, *k_out, *v_out;
+    int64_t heads;
+};
+
+cudaError_t launch_rms_modulate(const RowProblem &p, cudaStream_t s);
+cudaError_t launch_gated_rms_modulate(const RowProblem &p, cudaStream_t s);
+cudaError_t launch_ln_modulate(const RowProblem &p, cudaStream_t s);
+cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &p, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+} // namespace dan

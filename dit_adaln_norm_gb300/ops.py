@@ -1,0 +1,206 @@
+"""Thin ctypes binding of libdan.so (include/dan.h): argument marshalling only.
+
+Every function takes CUDA bf16 torch tensors, checks the layout the C ABI
+expects, passes raw pointers, strides and the current CUDA stream, and turns
+a non-zero status into an exception.  All arithmetic runs in the CUDA
+kernels; there is no CPU or eager fallback.  PyTorch only allocates outputs.
+
+The library is loaded on first use.  If it is missing the call raises
+(build it with ``python -c "import __graft_entry__ as g; g.build()"``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdan.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "dan.h")
+
+DAN_OK, DAN_EINVAL, DAN_EUNSUPPORTED, DAN_EALIGN, DAN_EALIAS, DAN_ECUDA = range(6)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_F = ctypes.c_float
+_SIGS = {
+    "dan_rms_modulate": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P],
+    "dan_can_use_rms_modulate": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _F],
+    "dan_gated_rms_modulate": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F, _P],
+    "dan_can_use_gated_rms_modulate": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F],
+    "dan_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F, _P],
+    "dan_can_use_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F],
+    "dan_qk_norm_rope_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
+                                  _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P],
+    "dan_can_use_qk_norm_rope_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
+                                          _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P],
+}
+
+_lib = None
+
+
+class DanError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def load():
+    """Load libdan.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdan.so not found at {LIB_PATH}: build the CUDA library first")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.dan_status_string.argtypes = [ctypes.c_int]
+        lib.dan_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/dan.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(dan_\w+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return load().dan_status_string(int(status)).decode()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != DAN_OK:
+        raise DanError(status, what)
+
+
+def _bf16_cuda(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+        raise TypeError(f"{name}: expected a CUDA bfloat16 tensor")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _rows(x: torch.Tensor, name: str):
+    _bf16_cuda(x, name)
+    if x.dim() != 3 or not x.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous [B, T, D] tensor")
+    return x.shape
+
+
+def _vectors(B: int, D: int, named):
+    """Per-batch [B, D] (or [D] when B == 1) views sharing one batch stride."""
+    strides = set()
+    for name, v in named:
+        _bf16_cuda(v, name)
+        if v.dim() == 1:
+            if B != 1 or v.shape[0] != D or v.stride(0) != 1:
+                raise ValueError(f"{name}: a 1-D vector needs B == 1, shape [D], unit stride")
+            strides.add(None)
+            continue
+        if tuple(v.shape) != (B, D) or v.stride(1) != 1:
+            raise ValueError(f"{name}: expected a [B={B}, D={D}] view with unit column stride")
+        strides.add(v.stride(0) if B > 1 else None)
+    strides.discard(None)
+    if len(strides) > 1:
+        raise ValueError("per-batch vectors must share one batch stride")
+    return strides.pop() if strides else D
+
+
+def _weight(w, D):
+    if w is None:
+        return None
+    _bf16_cuda(w, "weight")
+    if w.dim() != 1 or w.shape[0] != D or not w.is_contiguous():
+        raise ValueError("weight: expected a contiguous [D] tensor")
+    return w
+
+
+def rms_modulate(x, scale, shift, eps: float, weight=None, out=None):
+    """y = bf16(RMSNorm(x) [* weight] * (1 + scale) + shift), x [B, T, D]."""
+    B, T, D = _rows(x, "x")
+    vs = _vectors(B, D, [("scale", scale), ("shift", shift)])
+    weight = _weight(weight, D)
+    y = torch.empty_like(x) if out is None else out
+    _rows(y, "out")
+    _check(load().dan_rms_modulate(_ptr(x), _ptr(weight), _ptr(scale), _ptr(shift), vs, _ptr(y),
+                                   B, T, D, float(eps), _stream()), "dan_rms_modulate")
+    return y
+
+
+def gated_rms_modulate(r, h, gate, scale, shift, eps: float, weight=None, r_out=None, out=None):
+    """r' = bf16(r + bf16(gate * h)); y = rms_modulate(r').  Returns (r', y)."""
+    B, T, D = _rows(r, "r")
+    _rows(h, "h")
+    vs = _vectors(B, D, [("gate", gate), ("scale", scale), ("shift", shift)])
+    weight = _weight(weight, D)
+    r_out = torch.empty_like(r) if r_out is None else r_out
+    y = torch.empty_like(r) if out is None else out
+    _rows(r_out, "r_out")
+    _rows(y, "out")
+    _check(load().dan_gated_rms_modulate(_ptr(r), _ptr(h), _ptr(gate), _ptr(weight), _ptr(scale),
+                                         _ptr(shift), vs, _ptr(r_out), _ptr(y), B, T, D,
+                                         float(eps), _stream()), "dan_gated_rms_modulate")
+    return r_out, y
+
+
+def ln_modulate(x, scale, shift, eps: float, out=None):
+    """y = bf16(LayerNorm(x) * (1 + scale) + shift), LayerNorm without affine."""
+    B, T, D = _rows(x, "x")
+    vs = _vectors(B, D, [("scale", scale), ("shift", shift)])
+    y = torch.empty_like(x) if out is None else out
+    _rows(y, "out")
+    _check(load().dan_ln_modulate(_ptr(x), _ptr(scale), _ptr(shift), vs, _ptr(y), B, T, D,
+                                  float(eps), _stream()), "dan_ln_modulate")
+    return y
+
+
+def _qkv(views, name, heads):
+    q, k, v = views
+    T = q.shape[0]
+    for t, n in zip(views, "qkv"):
+        _bf16_cuda(t, f"{name}.{n}")
+        if t.dim() != 2 or t.shape != (T, heads * 128) or (T > 0 and t.stride(1) != 1):
+            raise ValueError(f"{name}.{n}: expected a [T, heads*128] view with unit column stride")
+    strides = {t.stride(0) for t in views} if T > 1 else {heads * 128}
+    if len(strides) != 1:
+        raise ValueError(f"{name}: q, k, v must share one row stride")
+    return T, strides.pop()
+
+
+def qk_norm_rope_epilogue(txt, img, wq_txt, wk_txt, wq_img, wk_img, rope_txt, rope_img,
+                          eps_txt: float, eps_img: float, heads: int, out=None):
+    """txt, img: (q, k, v) views [T_s, heads*128]; weights [128] bf16; rope
+    tables fp32 [T_s, 128].  Returns joint (q, k, v), each [T_txt+T_img, heads, 128]."""
+    Tt, st = _qkv(txt, "txt", heads)
+    Ti, si = _qkv(img, "img", heads)
+    for w, n in ((wq_txt, "wq_txt"), (wk_txt, "wk_txt"), (wq_img, "wq_img"), (wk_img, "wk_img")):
+        _bf16_cuda(w, n)
+        if w.shape != (128,) or not w.is_contiguous():
+            raise ValueError(f"{n}: expected a contiguous [128] tensor")
+    for r, n, T in ((rope_txt, "rope_txt", Tt), (rope_img, "rope_img", Ti)):
+        if not r.is_cuda or r.dtype != torch.float32 or r.shape != (T, 128) or not r.is_contiguous():
+            raise ValueError(f"{n}: expected a contiguous CUDA float32 [T, 128] tensor")
+    if out is None:
+        dev = txt[0].device
+        out = tuple(torch.empty((Tt + Ti, heads, 128), dtype=torch.bfloat16, device=dev)
+                    for _ in range(3))
+    qo, ko, vo = out
+    _check(load().dan_qk_norm_rope_epilogue(
+        _ptr(txt[0]), _ptr(txt[1]), _ptr(txt[2]), Tt, st,
+        _ptr(img[0]), _ptr(img[1]), _ptr(img[2]), Ti, si, heads, 128,
+        _ptr(wq_txt), _ptr(wk_txt), _ptr(wq_img), _ptr(wk_img), _ptr(rope_txt), _ptr(rope_img),
+        float(eps_txt), float(eps_img), _ptr(qo), _ptr(ko), _ptr(vo), _stream()),
+        "dan_qk_norm_rope_epilogue")
+    return qo, ko, vo

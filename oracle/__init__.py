@@ -168,6 +168,8 @@ def _qkv_views(q, k, v, name):
     """q, k, v: [T, H*128] views sharing one row stride (unit column stride)."""
     arrs = [_bits(a, f"{name}.{n}") for a, n in zip((q, k, v), "qkv")]
     T, HD = arrs[0].shape
+    if T == 0:  # an empty stream: nothing is read, strides are irrelevant
+        return [np.zeros((0, HD), np.uint16)] * 3, 0, HD, HD
     for a in arrs:
         if a.shape != (T, HD) or a.strides[1] != 2:
             raise ValueError(f"{name}: q, k, v must be [T, H*128] views, unit column stride")
