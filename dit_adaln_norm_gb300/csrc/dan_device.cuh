@@ -65,6 +65,17 @@ __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v)
                  : "memory");
 }
 
+// Asynchronous 16-byte global -> shared copy (bypassing L1), and the wait
+// for all of this thread's outstanding copies (a hardware wait on the
+// thread's own copy group, like a load dependency; no polling loop).
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
+{
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Read-only 16-byte load of a small broadcast vector (kept in L1/L2).
 __device__ __forceinline__ uint4 ld_vec(const uint4 *p) { return __ldg(p); }
 __device__ __forceinline__ float4 ld_vec(const float4 *p) { return __ldg(p); }

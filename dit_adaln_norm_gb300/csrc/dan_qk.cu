@@ -8,13 +8,14 @@
 // buffers; inputs are zero-copy row-strided views of the packed QKV GEMM
 // output (section 4).
 //
-// Work unit = (token, Q|K|V), one warp each, grid-stride over units.  A
-// half-warp covers one head: lane l (0..15) owns the 16-byte fragment of
+// Work unit = (token, Q|K|V, group of up to 24 heads), one warp each,
+// grid-stride over units.  A half-warp covers one head: lane l (0..15) owns the 16-byte fragment of
 // columns 8l..8l+7, so each head is one coalesced 256-byte load/store and
 // the two halves of a warp take adjacent heads (512 contiguous bytes).  The
 // per-token RoPE row and the stream's weight fragment are read once per unit.
 // Head RMS: each lane's 8 squares in column order, then the adjacent-pair
-// tree over the 16 lanes (xor 1,2,4,8 stays inside a half-warp).
+// tree over the 16 lanes (xor 1,2,4,8 stays inside a half-warp), done as a
+// recursive-halving fold so that each lane ends with one head's sum.
 #include "dan_device.cuh"
 #include "dan_internal.h"
 
@@ -22,81 +23,154 @@ namespace dan {
 
 struct QkParams {
     const uint4 *q[2], *k[2], *v[2];
-    int64_t T0;        // text tokens
-    int64_t T_all;     // text + image tokens
+    int64_t T0;         // text tokens
+    int64_t T_all;      // text + image tokens
     int64_t stride8[2]; // row stride in 16-byte fragments
     const uint4 *wq[2], *wk[2];
     const float4 *rope[2];
     float eps[2];
     uint4 *q_out, *k_out, *v_out;
     int H;
+    int groups; // head groups of kGroup heads per (token, kind)
 };
 
-constexpr int kQkWarps = 8;
-constexpr int kHeadsPerLane = 12; // heads held in registers per half-warp pass
+constexpr int kQkWarps = 12;
+constexpr int kHeadsPerLane = 12;           // heads a half-warp lane holds per unit
+constexpr int kGroup = 2 * kHeadsPerLane;   // heads per unit
 
-__global__ void __launch_bounds__(kQkWarps * 32) qk_norm_rope_kernel(const QkParams p)
+// One unit of work = (token, Q|K|V, group of up to kGroup heads), as
+// loaded registers: the head fragments plus, for Q and K, the weight
+// fragment and the token's cos/sin for this lane's four pairs.
+struct QkUnit {
+    uint4 x[kHeadsPerLane];
+    uint4 w;
+    float4 c4, s4;
+    int64_t tok;
+    int kind, h0, s;
+};
+
+__device__ __forceinline__ void qk_load(QkUnit &U, const QkParams &p, int64_t u, int half, int fl)
+{
+    const int64_t tg = u / 3;
+    U.kind = (int)(u - 3 * tg);
+    U.tok = tg / p.groups;
+    U.h0 = (int)(tg - U.tok * p.groups) * kGroup;
+    U.s = U.tok < p.T0 ? 0 : 1;
+    const int64_t t = U.s ? U.tok - p.T0 : U.tok;
+    const uint4 *src =
+        (U.kind == 0 ? p.q[U.s] : U.kind == 1 ? p.k[U.s] : p.v[U.s]) + t * p.stride8[U.s];
+#pragma unroll
+    for (int k = 0; k < kHeadsPerLane; ++k) {
+        const int h = U.h0 + half + 2 * k;
+        U.x[k] = h < p.H ? ld_stream(src + h * 16 + fl) : make_uint4(0, 0, 0, 0);
+    }
+    if (U.kind != 2) {
+        U.w = ld_vec((U.kind == 0 ? p.wq[U.s] : p.wk[U.s]) + fl);
+        U.c4 = ld_vec(p.rope[U.s] + t * 32 + fl);      // cos of pairs 4fl..4fl+3
+        U.s4 = ld_vec(p.rope[U.s] + t * 32 + 16 + fl); // sin of the same pairs
+    }
+}
+
+// Reverse the 4 low bits: after the halving fold, lane l holds head brev4(l).
+__device__ __forceinline__ int brev4(int l)
+{
+    return ((l & 1) << 3) | ((l & 2) << 1) | ((l & 4) >> 1) | ((l & 8) >> 3);
+}
+
+__device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, int half, int fl)
+{
+    uint4 *dst = (U.kind == 0 ? p.q_out : U.kind == 1 ? p.k_out : p.v_out) + U.tok * p.H * 16;
+    if (U.kind == 2) { // V: bit copy
+#pragma unroll
+        for (int k = 0; k < kHeadsPerLane; ++k) {
+            const int h = U.h0 + half + 2 * k;
+            if (h < p.H) st_stream(dst + h * 16 + fl, U.x[k]);
+        }
+        return;
+    }
+
+    // Partial sum of squares of each of the lane's heads over its 8 columns
+    // (one ordered chain per head; heads k, k+1 share packed multiplies).
+    float ps[16];
+#pragma unroll
+    for (int k = 0; k < kHeadsPerLane; k += 2) {
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float2 x2 = make_float2(elem(U.x[k], e), elem(U.x[k + 1], e));
+            acc = addmul2(acc, x2, x2);
+        }
+        ps[k] = acc.x;
+        ps[k + 1] = acc.y;
+    }
+#pragma unroll
+    for (int k = kHeadsPerLane; k < 16; ++k) ps[k] = 0.0f;
+
+    // Recursive-halving fold over the 16 lanes of the half-warp: at xor
+    // offset 1, 2, 4, 8 each lane keeps half of its heads and adds its
+    // partner's partial for them.  Per head this is exactly the adjacent-pair
+    // tree over the 16 lanes; afterwards lane fl holds the sum of head
+    // brev4(fl), so each lane computes one reciprocal square root.
+#pragma unroll
+    for (int lvl = 0, n = 16; lvl < 4; ++lvl, n >>= 1) {
+        const int off = 1 << lvl;
+        const bool upper = (fl & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = upper ? ps[i] : ps[i + n / 2];
+            const float keep = upper ? ps[i + n / 2] : ps[i];
+            ps[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
+        }
+    }
+    const float my_rstd = defined_rsqrt(__fadd_rn(__fdiv_rn(ps[0], 128.0f), p.eps[U.s]));
+
+    const float cs[4] = {U.c4.x, U.c4.y, U.c4.z, U.c4.w};
+    const float sn[4] = {U.s4.x, U.s4.y, U.s4.z, U.s4.w};
+    float2 w2[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) w2[m] = wide2(word(U.w, m));
+    const int lane_base = half << 4;
+#pragma unroll
+    for (int k = 0; k < kHeadsPerLane; ++k) {
+        const float rstd = __shfl_sync(kFull, my_rstd, lane_base + brev4(k));
+        if (U.h0 + 2 * k >= p.H) break; // warp-uniform: no head left for either half
+        const int h = U.h0 + half + 2 * k;
+        const float2 r2 = dup2(rstd);
+        uint4 out;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) { // pair i = 4fl + m: columns 2i, 2i+1
+            const float2 t2 = mul2(mul2(wide2(word(U.x[k], m)), r2), w2[m]);
+            const uint32_t n = pack_bf16(t2.x, t2.y);
+            const float a = lo_f(n), b = hi_f(n);
+            set_word(out, m,
+                     pack_bf16(__fsub_rn(__fmul_rn(a, cs[m]), __fmul_rn(b, sn[m])),
+                               __fadd_rn(__fmul_rn(a, sn[m]), __fmul_rn(b, cs[m]))));
+        }
+        if (h < p.H) st_stream(dst + h * 16 + fl, out);
+    }
+}
+
+// Warps walk units u = global warp, + total warps, ...; two register
+// buffers alternate so each warp has its next unit's loads in flight.
+__global__ void __launch_bounds__(kQkWarps * 32, 1) qk_norm_rope_kernel(const QkParams p)
 {
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, fl = lane & 15;
     const int64_t nwarps = (int64_t)gridDim.x * kQkWarps;
-    const int64_t units = 3 * p.T_all;
+    const int64_t units = 3 * p.T_all * p.groups;
 
-    for (int64_t u = (int64_t)blockIdx.x * kQkWarps + (threadIdx.x >> 5); u < units; u += nwarps) {
-        const int64_t tok = u / 3;
-        const int kind = (int)(u - 3 * tok); // 0 = Q, 1 = K, 2 = V
-        const int s = tok < p.T0 ? 0 : 1;
-        const int64_t t = s ? tok - p.T0 : tok;
-        const uint4 *src = (kind == 0 ? p.q[s] : kind == 1 ? p.k[s] : p.v[s]) + t * p.stride8[s];
-        uint4 *dst = (kind == 0 ? p.q_out : kind == 1 ? p.k_out : p.v_out) + tok * p.H * 16;
-
-        if (kind == 2) { // V: bit copy
-            for (int h = half; h < p.H; h += 2) st_stream(dst + h * 16 + fl, ld_stream(src + h * 16 + fl));
-            continue;
-        }
-
-        const uint4 w = ld_vec((kind == 0 ? p.wq[s] : p.wk[s]) + fl);
-        const float4 c4 = ld_vec(p.rope[s] + t * 32 + fl);      // cos of pairs 4fl..4fl+3
-        const float4 s4 = ld_vec(p.rope[s] + t * 32 + 16 + fl); // sin of the same pairs
-        const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
-        const float sn[4] = {s4.x, s4.y, s4.z, s4.w};
-        const float eps = p.eps[s];
-
-        for (int h0 = 0; h0 < p.H; h0 += 2 * kHeadsPerLane) {
-            uint4 x[kHeadsPerLane];
-#pragma unroll
-            for (int k = 0; k < kHeadsPerLane; ++k) {
-                const int h = h0 + half + 2 * k;
-                x[k] = h < p.H ? ld_stream(src + h * 16 + fl) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int k = 0; k < kHeadsPerLane; ++k) {
-                if (h0 + 2 * k >= p.H) break; // warp-uniform: no head left for either half
-                const int h = h0 + half + 2 * k;
-                float acc = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float xv = elem(x[k], e);
-                    acc = __fadd_rn(acc, __fmul_rn(xv, xv));
-                }
-#pragma unroll
-                for (int off = 1; off < 16; off <<= 1)
-                    acc = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, off));
-                const float rstd = defined_rsqrt(__fadd_rn(__fdiv_rn(acc, 128.0f), eps));
-                uint4 out;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) { // pair i = 4fl + m: columns 2i, 2i+1
-                    const uint32_t xw = word(x[k], m), ww = word(w, m);
-                    const uint32_t n = pack_bf16(__fmul_rn(__fmul_rn(lo_f(xw), rstd), lo_f(ww)),
-                                                 __fmul_rn(__fmul_rn(hi_f(xw), rstd), hi_f(ww)));
-                    const float a = lo_f(n), b = hi_f(n);
-                    set_word(out, m,
-                             pack_bf16(__fsub_rn(__fmul_rn(a, cs[m]), __fmul_rn(b, sn[m])),
-                                       __fadd_rn(__fmul_rn(a, sn[m]), __fmul_rn(b, cs[m]))));
-                }
-                if (h < p.H) st_stream(dst + h * 16 + fl, out);
-            }
-        }
+    QkUnit A, B;
+    int64_t ua = (int64_t)blockIdx.x * kQkWarps + (threadIdx.x >> 5), ub = ua + nwarps;
+    if (ua < units) qk_load(A, p, ua, half, fl);
+    if (ub < units) qk_load(B, p, ub, half, fl);
+    while (ua < units) {
+        qk_process(A, p, half, fl);
+        ua = ub + nwarps;
+        if (ua < units) qk_load(A, p, ua, half, fl);
+        if (ub >= units) break;
+        qk_process(B, p, half, fl);
+        ub = ua + nwarps;
+        if (ub < units) qk_load(B, p, ub, half, fl);
     }
 }
 
@@ -119,13 +193,18 @@ cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &q, cudaStream_t s)
     p.k_out = static_cast<uint4 *>(q.k_out);
     p.v_out = static_cast<uint4 *>(q.v_out);
     p.H = (int)q.heads;
+    p.groups = (int)((q.heads + kGroup - 1) / kGroup);
 
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qk_norm_rope_kernel, kQkWarps * 32,
-                                                      0) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    const int64_t units = 3 * p.T_all;
+    static int per_sm = 0; // resident CTAs per SM (a property of the kernel build)
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel, kQkWarps * 32,
+                                                          0) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        per_sm = n;
+    }
+    const int64_t units = 3 * p.T_all * p.groups;
     const int64_t want = (units + kQkWarps - 1) / kQkWarps;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const int grid = (int)(want < cap ? want : cap);

@@ -18,7 +18,9 @@
 //    modulated and stored; it is never re-read.
 //  - bf16(1 + scale), shift, gate and the norm weight are staged in shared
 //    memory once per CTA for every batch (when they fit), so the per-element
-//    work reads them with conflict-free 16-byte shared loads.
+//    work reads them with conflict-free 16-byte shared loads.  The staging
+//    copies are issued before the first rows' loads and completed after
+//    them, so the two overlap.
 //  - Canonical RMS order: logical thread tx (TPR = D/64 of them) owns the
 //    fragments TPR*b + tx (b = 0..7) as one sequential chain; lanes fold by
 //    the butterfly (= the adjacent-pair tree); logical warp sums fold by the
@@ -70,21 +72,40 @@ __device__ __forceinline__ uint4 vec_frag(const RowParams &p, const uint4 *s_vec
     return ld_vec((which == 1 ? p.shift : p.gate) + off);
 }
 
-// Stage the norm weight and bf16(1+scale), shift (, gate) of every batch.
+// Staging of the norm weight and of scale, shift (, gate) of every batch in
+// shared memory, in two halves around the first row loads: stage_begin
+// issues asynchronous copies (they enter the memory system ahead of the row
+// loads and hold no registers); stage_end waits for them, then rewrites
+// each scale fragment in place as bf16(1 + scale).
 template <int NV, bool HAS_W>
-__device__ __forceinline__ void stage_vectors(const RowParams &p, uint4 *s_w, uint4 *s_vec)
+__device__ __forceinline__ void stage_begin(const RowParams &p, uint4 *s_w, uint4 *s_vec)
 {
     const int F = p.F;
     if (HAS_W)
-        for (int f = threadIdx.x; f < F; f += blockDim.x) s_w[f] = ld_vec(p.weight + f);
+        for (int f = threadIdx.x; f < F; f += blockDim.x) cp_async16(s_w + f, p.weight + f);
     for (int i = threadIdx.x; i < p.Bs * F; i += blockDim.x) {
         const int b = i / F, f = i - b * F;
         const int64_t off = (int64_t)b * p.vs8 + f;
         uint4 *dst = s_vec + (int64_t)b * NV * F;
-        dst[f] = one_plus_fragment(ld_vec(p.scale + off));
-        dst[F + f] = ld_vec(p.shift + off);
-        if (NV == 3) dst[2 * F + f] = ld_vec(p.gate + off);
+        cp_async16(dst + f, p.scale + off);
+        cp_async16(dst + F + f, p.shift + off);
+        if (NV == 3) cp_async16(dst + 2 * F + f, p.gate + off);
     }
+    cp_async_commit();
+}
+
+template <int NV>
+__device__ __forceinline__ void stage_end(const RowParams &p, uint4 *s_vec)
+{
+    const int F = p.F;
+    cp_async_wait_all();
+    __syncthreads();
+    for (int i = threadIdx.x; i < p.Bs * F; i += blockDim.x) {
+        const int b = i / F, f = i - b * F;
+        uint4 *dst = s_vec + (int64_t)b * NV * F + f;
+        *dst = one_plus_fragment(*dst);
+    }
+    __syncthreads();
 }
 
 // Normalise + modulate one fragment of x with the row's rstd and store it.
@@ -109,20 +130,147 @@ __device__ __forceinline__ uint4 rms_out_fragment(const uint4 &xv, float rstd, c
 
 // ------------------------------------------------------------------ RMS
 
-// Two CTAs per SM (register cap 65536 / (2 * threads)): with one warp per
-// row this keeps 16 rows (128 KB at D = 4096) of loads in flight per SM.
-template <int LW, int PW, int WARPS, bool GATED, bool HAS_W>
-__global__ void __launch_bounds__(WARPS * 32, 2)
-    rms_modulate_kernel(const RowParams p)
+template <int LW, int PW, bool GATED>
+struct RmsRow {
+    uint4 v[LW][8];
+    uint4 h[GATED ? LW : 1][8];
+};
+
+// Issue the 16-byte loads of one row (x, and h for the gated form).
+template <int LW, int PW, bool GATED>
+__device__ __forceinline__ void rms_load(RmsRow<LW, PW, GATED> &b, const RowParams &p, int64_t row,
+                                         int pw, int lane)
 {
-    constexpr int WPR = LW * PW;  // logical warps per row
-    constexpr int TPR = 32 * WPR; // logical threads per row
-    constexpr int F = 8 * TPR;    // fragments per row
-    constexpr int D = 8 * F;
-    constexpr int RS = WARPS / PW; // row slots per CTA
+    constexpr int TPR = 32 * LW * PW, F = 8 * TPR;
+#pragma unroll
+    for (int j = 0; j < LW; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int f = TPR * k + 32 * (pw * LW + j) + lane;
+            b.v[j][k] = ld_stream(p.x + row * F + f);
+            if (GATED) b.h[j][k] = ld_stream(p.h + row * F + f);
+        }
+}
+
+// Gated residual (stored), canonical sum of squares, rstd, normalise,
+// modulate and store for one row whose data is in `b`.
+template <int LW, int PW, int WARPS, bool GATED, bool HAS_W>
+__device__ __forceinline__ void rms_process(RmsRow<LW, PW, GATED> &b, const RowParams &p,
+                                            int64_t row, const uint4 *s_w, const uint4 *s_vec,
+                                            float *s_red, int slot, int pw, int lane, int &parity)
+{
+    constexpr int WPR = LW * PW, TPR = 32 * WPR, F = 8 * TPR, D = 8 * F;
+    constexpr int RS = WARPS / PW;
     constexpr int NV = GATED ? 3 : 2;
     constexpr int P2 = WPR <= 1 ? 1 : WPR <= 2 ? 2 : WPR <= 4 ? 4 : 8;
     constexpr int NP = LW / 2; // packed chain pairs per lane
+    const int64_t bidx = row / p.T;
+
+    if (GATED) { // r' = bf16(r + bf16(gate * h)), stored, then normalised
+#pragma unroll
+        for (int j = 0; j < LW; ++j)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int f = TPR * k + 32 * (pw * LW + j) + lane;
+                const uint4 g = vec_frag<NV>(p, s_vec, bidx, f, 2);
+                uint4 &r = b.v[j][k];
+                const uint4 &hh = b.h[j][k];
+                r = make_uint4(gated_word(r.x, g.x, hh.x), gated_word(r.y, g.y, hh.y),
+                               gated_word(r.z, g.z, hh.z), gated_word(r.w, g.w, hh.w));
+                st_stream(p.r_out + row * F + f, r);
+            }
+    }
+
+    // Sum of squares: one ordered chain per logical thread (v fastest, then
+    // the fragment index); logical threads j, j+1 of a lane share packed
+    // multiplies.
+    float acc[LW];
+    {
+        float2 acc2[NP > 0 ? NP : 1];
+        float acc1 = 0.0f;
+#pragma unroll
+        for (int q = 0; q < NP; ++q) acc2[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const float2 x2 = make_float2(elem(b.v[2 * q][k], e), elem(b.v[2 * q + 1][k], e));
+                    acc2[q] = addmul2(acc2[q], x2, x2);
+                }
+                if (LW & 1) {
+                    const float xv = elem(b.v[LW - 1][k], e);
+                    acc1 = __fadd_rn(acc1, __fmul_rn(xv, xv));
+                }
+            }
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            acc[2 * q] = acc2[q].x;
+            acc[2 * q + 1] = acc2[q].y;
+        }
+        if (LW & 1) acc[LW - 1] = acc1;
+    }
+    // Adjacent-pair tree over the 32 lanes of each logical warp.
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < LW; ++j) acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(kFull, acc[j], off));
+
+    // Logical warp sums -> adjacent-pair tree padded with +0.
+    float t[P2];
+#pragma unroll
+    for (int k = 0; k < P2; ++k) t[k] = 0.0f;
+    if (PW == 1) {
+#pragma unroll
+        for (int j = 0; j < LW; ++j) t[j] = acc[j];
+    } else {
+        float *red = s_red + (parity * RS + slot) * WPR;
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < LW; ++j) red[pw * LW + j] = acc[j];
+        named_barrier(1 + slot, PW * 32);
+#pragma unroll
+        for (int k = 0; k < WPR; ++k) t[k] = red[k];
+        parity ^= 1;
+    }
+#pragma unroll
+    for (int off = 1; off < P2; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < P2; k += 2 * off) t[k] = __fadd_rn(t[k], t[k + off]);
+    const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(t[0], (float)D), p.eps)));
+
+#pragma unroll
+    for (int j = 0; j < LW; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int f = TPR * k + 32 * (pw * LW + j) + lane;
+            const uint4 o = vec_frag<NV>(p, s_vec, bidx, f, 0);
+            const uint4 sh = vec_frag<NV>(p, s_vec, bidx, f, 1);
+            uint4 wv = make_uint4(0, 0, 0, 0);
+            if (HAS_W) wv = s_w[f];
+            uint4 out;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                float2 t2 = mul2(wide2(word(b.v[j][k], w)), rstd2);
+                if (HAS_W) t2 = mul2(t2, wide2(word(wv, w)));
+                set_word(out, w, modulate_word(pack_bf16(t2.x, t2.y), word(o, w), word(sh, w)));
+            }
+            st_stream(p.y + row * F + f, out);
+        }
+}
+
+// Rows of a CTA are blockIdx.x + G*i (G = grid size); row slot s takes
+// i = s, s + RS, s + 2RS, ...  Two register buffers alternate: the loads of
+// a slot's next row are issued before its current row is processed, so
+// each warp keeps up to two rows in flight.
+template <int LW, int PW, int WARPS, int MINB, bool GATED, bool HAS_W>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+    rms_modulate_kernel(const RowParams p)
+{
+    constexpr int TPR = 32 * LW * PW, F = 8 * TPR;
+    constexpr int RS = WARPS / PW;
+    constexpr int NV = GATED ? 3 : 2;
 
     extern __shared__ uint4 smem[];
     uint4 *s_w = smem;
@@ -131,136 +279,26 @@ __global__ void __launch_bounds__(WARPS * 32, 2)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slot = warp / PW, pw = warp - slot * PW;
-    const int64_t G = gridDim.x;
+    const int64_t step = (int64_t)gridDim.x * RS;
 
-    uint4 v[LW][8];
-    uint4 hv[GATED ? LW : 1][8];
-
-    int64_t i = slot;
-    int64_t row = blockIdx.x + G * i;
-    // Issue the first row's loads before staging, so the two overlap.
-    if (row < p.rows) {
-#pragma unroll
-        for (int j = 0; j < LW; ++j)
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const int f = TPR * b + 32 * (pw * LW + j) + lane;
-                v[j][b] = ld_stream(p.x + row * F + f);
-                if (GATED) hv[j][b] = ld_stream(p.h + row * F + f);
-            }
-    }
-    stage_vectors<NV, HAS_W>(p, s_w, s_vec);
-    __syncthreads();
+    RmsRow<LW, PW, GATED> A, B;
+    int64_t ra = blockIdx.x + (int64_t)gridDim.x * slot, rb = ra + step;
+    stage_begin<NV, HAS_W>(p, s_w, s_vec);
+    if (ra < p.rows) rms_load(A, p, ra, pw, lane);
+    if (rb < p.rows) rms_load(B, p, rb, pw, lane);
+    stage_end<NV>(p, s_vec);
 
     int parity = 0;
-    while (row < p.rows) {
-        const int64_t bidx = row / p.T;
-
-        if (GATED) { // r' = bf16(r + bf16(gate * h)), stored, then normalised
-#pragma unroll
-            for (int j = 0; j < LW; ++j)
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    const int f = TPR * b + 32 * (pw * LW + j) + lane;
-                    const uint4 g = vec_frag<NV>(p, s_vec, bidx, f, 2);
-                    uint4 &r = v[j][b];
-                    const uint4 &hh = hv[j][b];
-                    r = make_uint4(gated_word(r.x, g.x, hh.x), gated_word(r.y, g.y, hh.y),
-                                   gated_word(r.z, g.z, hh.z), gated_word(r.w, g.w, hh.w));
-                    st_stream(p.r_out + row * F + f, r);
-                }
-        }
-
-        // Sum of squares: one ordered chain per logical thread (v fastest,
-        // then b); logical threads j, j+1 of a lane share packed operations.
-        float acc[LW];
-        {
-            float2 acc2[NP > 0 ? NP : 1];
-            float acc1 = 0.0f;
-#pragma unroll
-            for (int q = 0; q < NP; ++q) acc2[q] = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) {
-                        const float2 x2 = make_float2(elem(v[2 * q][b], e), elem(v[2 * q + 1][b], e));
-                        acc2[q] = addmul2(acc2[q], x2, x2);
-                    }
-                    if (LW & 1) {
-                        const float xv = elem(v[LW - 1][b], e);
-                        acc1 = __fadd_rn(acc1, __fmul_rn(xv, xv));
-                    }
-                }
-#pragma unroll
-            for (int q = 0; q < NP; ++q) {
-                acc[2 * q] = acc2[q].x;
-                acc[2 * q + 1] = acc2[q].y;
-            }
-            if (LW & 1) acc[LW - 1] = acc1;
-        }
-        // Adjacent-pair tree over the 32 lanes of each logical warp.
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1)
-#pragma unroll
-            for (int j = 0; j < LW; ++j)
-                acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(kFull, acc[j], off));
-
-        // Logical warp sums -> adjacent-pair tree padded with +0.
-        float t[P2];
-#pragma unroll
-        for (int k = 0; k < P2; ++k) t[k] = 0.0f;
-        if (PW == 1) {
-#pragma unroll
-            for (int j = 0; j < LW; ++j) t[j] = acc[j];
-        } else {
-            float *red = s_red + (parity * RS + slot) * WPR;
-            if (lane == 0)
-#pragma unroll
-                for (int j = 0; j < LW; ++j) red[pw * LW + j] = acc[j];
-            named_barrier(1 + slot, PW * 32);
-#pragma unroll
-            for (int k = 0; k < WPR; ++k) t[k] = red[k];
-            parity ^= 1;
-        }
-#pragma unroll
-        for (int off = 1; off < P2; off <<= 1)
-#pragma unroll
-            for (int k = 0; k < P2; k += 2 * off) t[k] = __fadd_rn(t[k], t[k + off]);
-        const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(t[0], (float)D), p.eps)));
-
-#pragma unroll
-        for (int j = 0; j < LW; ++j)
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                const int f = TPR * b + 32 * (pw * LW + j) + lane;
-                const uint4 o = vec_frag<NV>(p, s_vec, bidx, f, 0);
-                const uint4 sh = vec_frag<NV>(p, s_vec, bidx, f, 1);
-                uint4 wv = make_uint4(0, 0, 0, 0);
-                if (HAS_W) wv = s_w[f];
-                uint4 out;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    float2 t2 = mul2(wide2(word(v[j][b], w)), rstd2);
-                    if (HAS_W) t2 = mul2(t2, wide2(word(wv, w)));
-                    set_word(out, w, modulate_word(pack_bf16(t2.x, t2.y), word(o, w), word(sh, w)));
-                }
-                st_stream(p.y + row * F + f, out);
-            }
-
-        i += RS;
-        row = blockIdx.x + G * i;
-        if (row < p.rows) {
-#pragma unroll
-            for (int j = 0; j < LW; ++j)
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    const int f = TPR * b + 32 * (pw * LW + j) + lane;
-                    v[j][b] = ld_stream(p.x + row * F + f);
-                    if (GATED) hv[j][b] = ld_stream(p.h + row * F + f);
-                }
-        }
+    while (ra < p.rows) {
+        rms_process<LW, PW, WARPS, GATED, HAS_W>(A, p, ra, s_w, s_vec, s_red, slot, pw, lane,
+                                                 parity);
+        ra = rb + step;
+        if (ra < p.rows) rms_load(A, p, ra, pw, lane);
+        if (rb >= p.rows) break;
+        rms_process<LW, PW, WARPS, GATED, HAS_W>(B, p, rb, s_w, s_vec, s_red, slot, pw, lane,
+                                                 parity);
+        rb = ra + step;
+        if (rb < p.rows) rms_load(B, p, rb, pw, lane);
     }
 }
 
@@ -324,191 +362,210 @@ struct InvTable2 {
     float2 v[65];
 };
 
+template <int LW, int FPT>
+struct LnRow {
+    uint4 v[LW][FPT];
+};
+
+// fragment index of logical thread (warp pw, chain j, lane), k-th visit
+template <int LW>
+__device__ __forceinline__ int ln_frag(int pw, int j, int lane, int k)
+{
+    return 32 * (pw * LW + j) + lane + 128 * k;
+}
+
+template <int LW, int FPT, bool RAGGED>
+__device__ __forceinline__ void ln_load(LnRow<LW, FPT> &b, const RowParams &p, int64_t row, int pw,
+                                        int lane)
+{
+    const int F = p.F;
+#pragma unroll
+    for (int j = 0; j < LW; ++j)
+#pragma unroll
+        for (int k = 0; k < FPT; ++k) {
+            const int f = ln_frag<LW>(pw, j, lane, k);
+            b.v[j][k] = (!RAGGED || f < F) ? ld_stream(p.x + row * F + f) : make_uint4(0, 0, 0, 0);
+        }
+}
+
 template <int LW, int PW, int FPT, bool RAGGED, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32, 2)
-    ln_modulate_kernel(const RowParams p, const InvTable2 inv)
+__device__ __forceinline__ void ln_process(LnRow<LW, FPT> &b, const RowParams &p, int64_t row,
+                                           const InvTable2 &inv, const uint4 *s_vec, float *s_red,
+                                           int slot, int pw, int lane, int &parity)
 {
     constexpr int RS = WARPS / PW;
     constexpr int NV = 2;
     constexpr int NQ = LW / 2; // packed chain pairs per lane (LW is 2 or 4)
+    const int F = p.F;
+    const int64_t bidx = row / p.T;
+    // Statistics of the lane's logical warps: (mean, m2) of logical warp
+    // pw*LW + j, already folded over its 32 threads.
+    float wmean[LW], wm2[LW];
+
+    if (!RAGGED) {
+        // Every logical thread holds FPT full fragments: counts are equal
+        // everywhere, so each combine has c = 1/2 exactly.
+        float2 mean2[NQ], m22[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) mean2[q] = m22[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < FPT; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float2 r = inv.v[8 * k + e + 1];
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const float2 x2 = make_float2(elem(b.v[2 * q][k], e), elem(b.v[2 * q + 1][k], e));
+                    const float2 d = sub2(x2, mean2[q]);
+                    mean2[q] = addmul2(mean2[q], d, r);
+                    m22[q] = addmul2(m22[q], d, sub2(x2, mean2[q]));
+                }
+            }
+        float nA = (float)(8 * FPT);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float2 mb = make_float2(__shfl_down_sync(kFull, mean2[q].x, off),
+                                              __shfl_down_sync(kFull, mean2[q].y, off));
+                const float2 m2b = make_float2(__shfl_down_sync(kFull, m22[q].x, off),
+                                               __shfl_down_sync(kFull, m22[q].y, off));
+                combine_eq2(mean2[q], m22[q], mb, m2b, nA);
+            }
+            nA = 2.0f * nA;
+        }
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            wmean[2 * q] = __shfl_sync(kFull, mean2[q].x, 0);
+            wmean[2 * q + 1] = __shfl_sync(kFull, mean2[q].y, 0);
+            wm2[2 * q] = __shfl_sync(kFull, m22[q].x, 0);
+            wm2[2 * q + 1] = __shfl_sync(kFull, m22[q].y, 0);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < LW; ++j) {
+            float mean = 0.0f, m2 = 0.0f;
+            int nfr = 0;
+#pragma unroll
+            for (int k = 0; k < FPT; ++k) {
+                if (ln_frag<LW>(pw, j, lane, k) < F) {
+                    nfr = k + 1;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float xv = elem(b.v[j][k], e);
+                        const float d = __fsub_rn(xv, mean);
+                        mean = __fadd_rn(mean, __fmul_rn(d, inv.v[8 * k + e + 1].x));
+                        m2 = __fadd_rn(m2, __fmul_rn(d, __fsub_rn(xv, mean)));
+                    }
+                }
+            }
+            Welford st{(float)(8 * nfr), mean, m2};
+            st = warp_fold(st, lane);
+            wmean[j] = st.mean;
+            wm2[j] = st.m2;
+        }
+    }
+
+    // The four logical warps: (W0 + W2) + (W1 + W3).
+    float M[4], Q[4];
+    if (PW == 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            M[j] = wmean[j];
+            Q[j] = wm2[j];
+        }
+    } else {
+        float *red = s_red + (parity * RS + slot) * 8;
+        if (lane == 0)
+#pragma unroll
+            for (int j = 0; j < LW; ++j) {
+                red[2 * (pw * LW + j) + 0] = wmean[j];
+                red[2 * (pw * LW + j) + 1] = wm2[j];
+            }
+        named_barrier(1 + slot, PW * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            M[j] = red[2 * j];
+            Q[j] = red[2 * j + 1];
+        }
+        parity ^= 1;
+    }
+    float mean, m2;
+    if (!RAGGED) {
+        const float nw = (float)(256 * FPT); // count of one logical warp
+        float2 m01 = make_float2(M[0], M[1]), q01 = make_float2(Q[0], Q[1]);
+        combine_eq2(m01, q01, make_float2(M[2], M[3]), make_float2(Q[2], Q[3]), nw);
+        mean = m01.x;
+        m2 = q01.x;
+        combine_eq1(mean, m2, m01.y, q01.y, 2.0f * nw);
+    } else {
+        float N[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // count of logical warp j: 8 per valid fragment of its threads
+            int cnt = 0;
+            for (int t = 32 * j; t < 32 * j + 32; ++t)
+                for (int k = 0; k < FPT; ++k) cnt += (t + 128 * k < F) ? 8 : 0;
+            N[j] = (float)cnt;
+        }
+        const Welford S = combine(combine(Welford{N[0], M[0], Q[0]}, Welford{N[2], M[2], Q[2]}),
+                                  combine(Welford{N[1], M[1], Q[1]}, Welford{N[3], M[3], Q[3]}));
+        mean = S.mean;
+        m2 = S.m2;
+    }
+    const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
+    const float2 mean2 = dup2(mean);
+
+#pragma unroll
+    for (int j = 0; j < LW; ++j)
+#pragma unroll
+        for (int k = 0; k < FPT; ++k) {
+            const int f = ln_frag<LW>(pw, j, lane, k);
+            if (RAGGED && f >= F) continue;
+            const uint4 o = vec_frag<NV>(p, s_vec, bidx, f, 0);
+            const uint4 sh = vec_frag<NV>(p, s_vec, bidx, f, 1);
+            uint4 out;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float2 t2 = mul2(sub2(wide2(word(b.v[j][k], w)), mean2), rstd2);
+                set_word(out, w, modulate_word(pack_bf16(t2.x, t2.y), word(o, w), word(sh, w)));
+            }
+            st_stream(p.y + row * F + f, out);
+        }
+}
+
+// Same row schedule and two-buffer pipeline as the RMS kernel.
+template <int LW, int PW, int FPT, bool RAGGED, int WARPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB)
+    ln_modulate_kernel(const RowParams p, const InvTable2 inv)
+{
+    constexpr int RS = WARPS / PW;
+    constexpr int NV = 2;
 
     extern __shared__ uint4 smem[];
     uint4 *s_vec = smem;
-    const int F = p.F;
-    float *s_red = reinterpret_cast<float *>(s_vec + (int64_t)p.Bs * NV * F);
+    float *s_red = reinterpret_cast<float *>(s_vec + (int64_t)p.Bs * NV * p.F);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slot = warp / PW, pw = warp - slot * PW;
-    const int64_t G = gridDim.x;
+    const int64_t step = (int64_t)gridDim.x * RS;
 
-    // fragment of logical thread (j, lane), k-th visit: t + 128k
-    auto frag = [&](int j, int k) { return 32 * (pw * LW + j) + lane + 128 * k; };
-
-    uint4 v[LW][FPT];
-    int64_t i = slot;
-    int64_t row = blockIdx.x + G * i;
-    if (row < p.rows) {
-#pragma unroll
-        for (int j = 0; j < LW; ++j)
-#pragma unroll
-            for (int k = 0; k < FPT; ++k) {
-                const int f = frag(j, k);
-                v[j][k] = (!RAGGED || f < F) ? ld_stream(p.x + row * F + f) : make_uint4(0, 0, 0, 0);
-            }
-    }
-    stage_vectors<NV, false>(p, nullptr, s_vec);
-    __syncthreads();
+    LnRow<LW, FPT> A, B;
+    int64_t ra = blockIdx.x + (int64_t)gridDim.x * slot, rb = ra + step;
+    stage_begin<NV, false>(p, nullptr, s_vec);
+    if (ra < p.rows) ln_load<LW, FPT, RAGGED>(A, p, ra, pw, lane);
+    if (rb < p.rows) ln_load<LW, FPT, RAGGED>(B, p, rb, pw, lane);
+    stage_end<NV>(p, s_vec);
 
     int parity = 0;
-    while (row < p.rows) {
-        const int64_t bidx = row / p.T;
-        // Statistics of the lane's logical warps: W[j] = (mean, m2) of
-        // logical warp pw*LW + j, already folded over its 32 threads.
-        float wmean[LW], wm2[LW];
-
-        if (!RAGGED) {
-            // Every logical thread holds FPT full fragments: counts are
-            // equal everywhere, so each combine has c = 1/2 exactly.
-            float2 mean2[NQ], m22[NQ];
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) mean2[q] = m22[q] = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int k = 0; k < FPT; ++k)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float2 r = inv.v[8 * k + e + 1];
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q) {
-                        const float2 x2 =
-                            make_float2(elem(v[2 * q][k], e), elem(v[2 * q + 1][k], e));
-                        const float2 d = sub2(x2, mean2[q]);
-                        mean2[q] = addmul2(mean2[q], d, r);
-                        m22[q] = addmul2(m22[q], d, sub2(x2, mean2[q]));
-                    }
-                }
-            float nA = (float)(8 * FPT);
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const float2 mb = make_float2(__shfl_down_sync(kFull, mean2[q].x, off),
-                                                  __shfl_down_sync(kFull, mean2[q].y, off));
-                    const float2 m2b = make_float2(__shfl_down_sync(kFull, m22[q].x, off),
-                                                   __shfl_down_sync(kFull, m22[q].y, off));
-                    combine_eq2(mean2[q], m22[q], mb, m2b, nA);
-                }
-                nA = 2.0f * nA;
-            }
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                wmean[2 * q] = __shfl_sync(kFull, mean2[q].x, 0);
-                wmean[2 * q + 1] = __shfl_sync(kFull, mean2[q].y, 0);
-                wm2[2 * q] = __shfl_sync(kFull, m22[q].x, 0);
-                wm2[2 * q + 1] = __shfl_sync(kFull, m22[q].y, 0);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < LW; ++j) {
-                float mean = 0.0f, m2 = 0.0f;
-                int nfr = 0;
-#pragma unroll
-                for (int k = 0; k < FPT; ++k) {
-                    if (frag(j, k) < F) {
-                        nfr = k + 1;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float xv = elem(v[j][k], e);
-                            const float d = __fsub_rn(xv, mean);
-                            mean = __fadd_rn(mean, __fmul_rn(d, inv.v[8 * k + e + 1].x));
-                            m2 = __fadd_rn(m2, __fmul_rn(d, __fsub_rn(xv, mean)));
-                        }
-                    }
-                }
-                Welford st{(float)(8 * nfr), mean, m2};
-                st = warp_fold(st, lane);
-                wmean[j] = st.mean;
-                wm2[j] = st.m2;
-            }
-        }
-
-        // The four logical warps: (W0 + W2) + (W1 + W3).
-        float M[4], Q[4], N[4];
-        if (PW == 1) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                M[j] = wmean[j];
-                Q[j] = wm2[j];
-            }
-        } else {
-            float *red = s_red + (parity * RS + slot) * 8;
-            if (lane == 0)
-#pragma unroll
-                for (int j = 0; j < LW; ++j) {
-                    red[2 * (pw * LW + j) + 0] = wmean[j];
-                    red[2 * (pw * LW + j) + 1] = wm2[j];
-                }
-            named_barrier(1 + slot, PW * 32);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                M[j] = red[2 * j];
-                Q[j] = red[2 * j + 1];
-            }
-            parity ^= 1;
-        }
-        float mean, m2;
-        if (!RAGGED) {
-            const float nw = (float)(256 * FPT); // count of one logical warp
-            float2 m01 = make_float2(M[0], M[1]), q01 = make_float2(Q[0], Q[1]);
-            combine_eq2(m01, q01, make_float2(M[2], M[3]), make_float2(Q[2], Q[3]), nw);
-            mean = m01.x;
-            m2 = q01.x;
-            combine_eq1(mean, m2, m01.y, q01.y, 2.0f * nw);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                // count of logical warp j: 8 per valid fragment of its threads
-                int cnt = 0;
-                for (int t = 32 * j; t < 32 * j + 32; ++t)
-                    for (int k = 0; k < FPT; ++k) cnt += (t + 128 * k < F) ? 8 : 0;
-                N[j] = (float)cnt;
-            }
-            const Welford S = combine(combine(Welford{N[0], M[0], Q[0]}, Welford{N[2], M[2], Q[2]}),
-                                      combine(Welford{N[1], M[1], Q[1]}, Welford{N[3], M[3], Q[3]}));
-            mean = S.mean;
-            m2 = S.m2;
-        }
-        const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
-        const float2 mean2 = dup2(mean);
-
-#pragma unroll
-        for (int j = 0; j < LW; ++j)
-#pragma unroll
-            for (int k = 0; k < FPT; ++k) {
-                const int f = frag(j, k);
-                if (RAGGED && f >= F) continue;
-                const uint4 o = vec_frag<NV>(p, s_vec, bidx, f, 0);
-                const uint4 sh = vec_frag<NV>(p, s_vec, bidx, f, 1);
-                uint4 out;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float2 t2 = mul2(sub2(wide2(word(v[j][k], w)), mean2), rstd2);
-                    set_word(out, w, modulate_word(pack_bf16(t2.x, t2.y), word(o, w), word(sh, w)));
-                }
-                st_stream(p.y + row * F + f, out);
-            }
-
-        i += RS;
-        row = blockIdx.x + G * i;
-        if (row < p.rows) {
-#pragma unroll
-            for (int j = 0; j < LW; ++j)
-#pragma unroll
-                for (int k = 0; k < FPT; ++k) {
-                    const int f = frag(j, k);
-                    v[j][k] = (!RAGGED || f < F) ? ld_stream(p.x + row * F + f)
-                                                 : make_uint4(0, 0, 0, 0);
-                }
-        }
+    while (ra < p.rows) {
+        ln_process<LW, PW, FPT, RAGGED, WARPS>(A, p, ra, inv, s_vec, s_red, slot, pw, lane, parity);
+        ra = rb + step;
+        if (ra < p.rows) ln_load<LW, FPT, RAGGED>(A, p, ra, pw, lane);
+        if (rb >= p.rows) break;
+        ln_process<LW, PW, FPT, RAGGED, WARPS>(B, p, rb, inv, s_vec, s_red, slot, pw, lane, parity);
+        rb = ra + step;
+        if (rb < p.rows) ln_load<LW, FPT, RAGGED>(B, p, rb, pw, lane);
     }
 }
 
@@ -588,7 +645,7 @@ cudaError_t launch(K fn, int warps, int row_slots, const RowParams &p, int smem,
     return cudaGetLastError();
 }
 
-template <int LW, int PW, int WARPS, bool GATED>
+template <int LW, int PW, int WARPS, int MINB, bool GATED>
 cudaError_t launch_rms_t(const RowProblem &q, cudaStream_t s)
 {
     constexpr int NV = GATED ? 3 : 2;
@@ -597,15 +654,18 @@ cudaError_t launch_rms_t(const RowProblem &q, cudaStream_t s)
     const int smem = (int)((has_w ? q.D * 2 : 0) + (int64_t)p.Bs * NV * q.D * 2 +
                            (PW > 1 ? 2 * (WARPS / PW) * LW * PW * 4 : 0));
     if (has_w)
-        return launch(rms_modulate_kernel<LW, PW, WARPS, GATED, true>, WARPS, WARPS / PW, p, smem,
-                      s);
-    return launch(rms_modulate_kernel<LW, PW, WARPS, GATED, false>, WARPS, WARPS / PW, p, smem, s);
+        return launch(rms_modulate_kernel<LW, PW, WARPS, MINB, GATED, true>, WARPS, WARPS / PW, p,
+                      smem, s);
+    return launch(rms_modulate_kernel<LW, PW, WARPS, MINB, GATED, false>, WARPS, WARPS / PW, p,
+                  smem, s);
 }
 
 template <int LW, int PW, int FPT, bool RAGGED>
 cudaError_t launch_ln_t(const RowProblem &q, cudaStream_t s)
 {
-    constexpr int WARPS = 8;
+    // two row buffers of LW * FPT fragments: 12 warps per SM up to 4096
+    constexpr int WARPS = FPT <= 2 ? 16 : 12;
+    constexpr int MINB = 1;
     const RowParams p = make_params(q, 2);
     InvTable2 inv;
     inv.v[0] = make_float2(0.0f, 0.0f);
@@ -614,8 +674,8 @@ cudaError_t launch_ln_t(const RowProblem &q, cudaStream_t s)
         inv.v[n] = make_float2(r, r);
     }
     const int smem = (int)((int64_t)p.Bs * 2 * q.D * 2 + (PW > 1 ? 2 * (WARPS / PW) * 8 * 4 : 0));
-    return launch(ln_modulate_kernel<LW, PW, FPT, RAGGED, WARPS>, WARPS, WARPS / PW, p, smem, s,
-                  inv);
+    return launch(ln_modulate_kernel<LW, PW, FPT, RAGGED, WARPS, MINB>, WARPS, WARPS / PW, p, smem,
+                  s, inv);
 }
 
 template <bool RAGGED>
@@ -635,23 +695,25 @@ cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
 
 } // namespace
 
+// Configurations (logical warps per warp, warps per row, warps per CTA,
+// CTAs per SM): chosen so that the two row buffers fit the register file.
 cudaError_t launch_rms_modulate(const RowProblem &q, cudaStream_t s)
 {
     switch (q.D) {
-    case 2048: return launch_rms_t<1, 1, 8, false>(q, s);
-    case 4096: return launch_rms_t<2, 1, 8, false>(q, s);
-    case 6144: return launch_rms_t<1, 3, 12, false>(q, s);
-    default: return launch_rms_t<2, 2, 8, false>(q, s); // 8192
+    case 2048: return launch_rms_t<1, 1, 8, 2, false>(q, s);
+    case 4096: return launch_rms_t<2, 1, 12, 1, false>(q, s);
+    case 6144: return launch_rms_t<1, 3, 12, 1, false>(q, s);
+    default: return launch_rms_t<2, 2, 12, 1, false>(q, s); // 8192
     }
 }
 
 cudaError_t launch_gated_rms_modulate(const RowProblem &q, cudaStream_t s)
 {
     switch (q.D) {
-    case 2048: return launch_rms_t<1, 1, 8, true>(q, s);
-    case 4096: return launch_rms_t<1, 2, 8, true>(q, s);
-    case 6144: return launch_rms_t<1, 3, 12, true>(q, s);
-    default: return launch_rms_t<1, 4, 8, true>(q, s); // 8192
+    case 2048: return launch_rms_t<1, 1, 8, 2, true>(q, s);
+    case 4096: return launch_rms_t<1, 2, 12, 1, true>(q, s);
+    case 6144: return launch_rms_t<1, 3, 12, 1, true>(q, s);
+    default: return launch_rms_t<1, 4, 12, 1, true>(q, s); // 8192
     }
 }
 
