@@ -73,6 +73,17 @@ def aggregate(elapsed_max_s: float, steps: int, world: int):
             "ms_per_step": elapsed_max_s * 1e3 / steps}
 
 
+def max_over_ranks(v: float, dist=None, device="cpu") -> float:
+    """The largest of the ranks' values (the slowest rank's elapsed time);
+    `dist` is torch.distributed (NCCL on GPUs, gloo on CPU) or None."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -436,17 +447,9 @@ def run_ours(args, rank, world, dist):
             barrier()
         e2e = (e2e_el, e2e_steps, h2d, d2h)
 
-    # max over ranks
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    elapsed = max_over_ranks(elapsed)
+    elapsed = max_over_ranks(elapsed, dist, dev)
     if e2e is not None:
-        e2e = (max_over_ranks(e2e[0]),) + e2e[1:]
+        e2e = (max_over_ranks(e2e[0], dist, dev),) + e2e[1:]
     if rank != 0:
         return
 

@@ -1,0 +1,117 @@
+"""Batch invariance on the GPU: a row's output bits do not depend on the batch
+it is computed in, the token count, padding or the launch shape.
+
+LayerNorm+modulate at D=4096 as a classifier-free-guidance batch (B=2,
+T=1140, per-batch scale/shift ~ N(0, 0.2)) is recomputed at B=1 per batch,
+row by row (T=1, one launch per row), as one launch of 2280 single-row
+batches (vectors read from global memory), and with T padded to 1152
+(random pad rows, ignored); every variant must match the full run and the
+oracle bit for bit.  The same holds for RMSNorm, the gated form and the QK
+epilogue (token subsets of the joint run)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dit_adaln_norm_gb300 import ops, synth
+from _gpu import assert_bits_equal, from_dev, to_dev
+
+pytestmark = pytest.mark.gpu
+EPS = 1e-6
+B, T, TP, D = 2, 1140, 1152, 4096
+
+
+@pytest.fixture(scope="module")
+def cfg_inputs():
+    x = synth.outlier_rows_bf16((B, T, D), synth.SEED_X, synth.SEED_OUTLIER)
+    vec = synth.normal_bf16((B, 6 * D), synth.SEED_VEC, 0.2)
+    sc, sh = vec[:, :D], vec[:, D:2 * D]
+    return x, sc, sh
+
+
+def _variants(fn, x, sc, sh):
+    """Outputs [B, T, D] of fn(x, scale, shift) for each batch composition."""
+    dsc, dsh = to_dev(np.ascontiguousarray(sc)), to_dev(np.ascontiguousarray(sh))
+    out = {"full": from_dev(fn(to_dev(x), dsc, dsh))}
+    out["per_batch"] = np.stack([from_dev(fn(to_dev(x[b:b + 1]), dsc[b:b + 1], dsh[b:b + 1]))[0]
+                                 for b in range(B)])
+    rows = np.empty_like(x)
+    for b in range(B):
+        xb = to_dev(x[b:b + 1])
+        for t in range(T):
+            rows[b, t] = from_dev(fn(xb[:, t:t + 1].contiguous(), dsc[b:b + 1], dsh[b:b + 1]))[0, 0]
+    out["row_by_row"] = rows
+    # one launch, every row its own batch (B*T batches of T=1)
+    idx = np.repeat(np.arange(B), T)
+    many = fn(to_dev(x.reshape(B * T, 1, D)), dsc[idx], dsh[idx])
+    out["single_row_batches"] = from_dev(many).reshape(B, T, D)
+    # padded token count
+    xp = synth.normal_bf16((B, TP, D), 77, 3.0)
+    xp[:, :T] = x
+    out["padded"] = from_dev(fn(to_dev(xp), dsc, dsh))[:, :T]
+    return out
+
+
+def test_ln_cfg_batch_invariance(cfg_inputs):
+    x, sc, sh = cfg_inputs
+    want = oracle.ln_modulate(x, sc, sh, EPS)
+    outs = _variants(lambda a, s, h: ops.ln_modulate(a, s, h, EPS), x, sc, sh)
+    for name, y in outs.items():
+        assert_bits_equal(y, want, f"ln {name}")
+
+
+def test_rms_batch_invariance(cfg_inputs):
+    x, sc, sh = cfg_inputs
+    want = oracle.rms_modulate(x, sc, sh, EPS)
+    outs = _variants(lambda a, s, h: ops.rms_modulate(a, s, h, EPS), x, sc, sh)
+    for name, y in outs.items():
+        assert_bits_equal(y, want, f"rms {name}")
+
+
+def test_gated_batch_invariance(cfg_inputs):
+    x, sc, sh = cfg_inputs
+    sc, sh = np.ascontiguousarray(sc), np.ascontiguousarray(sh)  # one batch stride with gate
+    h = synth.normal_bf16((B, T, D), 5)
+    gate = synth.normal_bf16((B, D), 6, 0.1)
+    want_r, want_y = oracle.gated_rms_modulate(x, h, gate, sc, sh, EPS)
+    dg = to_dev(gate)
+    full_r, full_y = ops.gated_rms_modulate(to_dev(x), to_dev(h), dg, to_dev(np.ascontiguousarray(sc)),
+                                            to_dev(np.ascontiguousarray(sh)), EPS)
+    assert_bits_equal(from_dev(full_r), want_r, "gated r' full")
+    assert_bits_equal(from_dev(full_y), want_y, "gated y full")
+    for b in range(B):  # per batch, and a token subset of one batch
+        for t0, t1 in ((0, T), (17, 530)):
+            r_b, y_b = ops.gated_rms_modulate(
+                to_dev(x[b:b + 1, t0:t1]), to_dev(h[b:b + 1, t0:t1]), dg[b:b + 1],
+                to_dev(np.ascontiguousarray(sc[b:b + 1])), to_dev(np.ascontiguousarray(sh[b:b + 1])),
+                EPS)
+            assert_bits_equal(from_dev(r_b)[0], want_r[b, t0:t1], f"gated r' b={b} [{t0},{t1})")
+            assert_bits_equal(from_dev(y_b)[0], want_y[b, t0:t1], f"gated y b={b} [{t0},{t1})")
+
+
+def test_qk_token_subsets_match_joint_run():
+    H, Tt, Ti = 24, 256, 1024
+    pt, pi = synth.packed_qkv(Tt, H, 90), synth.packed_qkv(Ti, H, 91)
+    ws = synth.head_weights(4, 92)
+    rt, ri = synth.rope_table(Tt), synth.rope_table(Ti, pos0=Tt)
+    dw = [to_dev(w) for w in ws]
+    Pt, Pi = to_dev(pt), to_dev(pi)
+    RT, RI = torch.from_numpy(rt).cuda(), torch.from_numpy(ri).cuda()
+    full = [from_dev(o) for o in ops.qk_norm_rope_epilogue(
+        synth.split_qkv(Pt, H), synth.split_qkv(Pi, H), *dw, RT, RI, EPS, EPS, H)]
+    want = oracle.qk_norm_rope_epilogue(synth.split_qkv(pt, H), synth.split_qkv(pi, H), H, ws,
+                                        rt, ri, EPS, EPS)
+    for g, w in zip(full, want):
+        assert_bits_equal(g, w, "qk joint")
+    # image tokens alone (empty text stream), and a slice of each stream
+    empty = synth.split_qkv(Pt[:0], H)
+    img_only = [from_dev(o) for o in ops.qk_norm_rope_epilogue(
+        empty, synth.split_qkv(Pi, H), *dw, RT[:0], RI, EPS, EPS, H)]
+    for g, f in zip(img_only, full):
+        assert_bits_equal(g, f[Tt:], "qk image only")
+    a, b, c, d = 31, 200, 100, 900
+    part = [from_dev(o) for o in ops.qk_norm_rope_epilogue(
+        synth.split_qkv(Pt[a:b], H), synth.split_qkv(Pi[c:d], H), *dw, RT[a:b].contiguous(),
+        RI[c:d].contiguous(), EPS, EPS, H)]
+    for g, f in zip(part, full):
+        assert_bits_equal(g, np.concatenate([f[a:b], f[Tt + c:Tt + d]]), "qk token slices")
