@@ -183,6 +183,24 @@ int launched(cudaError_t e) { return e == cudaSuccess ? DAN_OK : DAN_ECUDA; }
 
 namespace dan {
 
+// The status word of each device the library runs on (a static device
+// variable: one instance per device, never allocated by the library).
+__device__ unsigned int g_device_status;
+
+unsigned *device_status()
+{
+    static unsigned *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    unsigned *&c = cache[dev & 63];
+    if (c == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
+        c = static_cast<unsigned *>(ptr);
+    }
+    return c;
+}
+
 int sm_count()
 {
     static int cache[64] = {0};
@@ -201,6 +219,23 @@ int sm_count()
 } // namespace dan
 
 extern "C" {
+
+int dan_get_device_status(unsigned int *status)
+{
+    if (!status) return DAN_EINVAL;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, dan::g_device_status, sizeof v) != cudaSuccess) return DAN_ECUDA;
+    if (cudaMemcpyToSymbol(dan::g_device_status, &zero, sizeof zero) != cudaSuccess) return DAN_ECUDA;
+    *status = v;
+    return DAN_OK;
+}
+
+int dan_selftest_wait_timeout(unsigned long long limit_ns, void *stream)
+{
+    if (limit_ns == 0 || limit_ns > 2000000000ull) return DAN_EINVAL;
+    if (!dan::device_status()) return DAN_ECUDA;
+    return launched(dan::launch_wait_selftest(limit_ns, static_cast<cudaStream_t>(stream)));
+}
 
 const char *dan_status_string(int status)
 {

@@ -41,4 +41,11 @@ cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &p, cudaStream_t s);
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Device address of the current device's status word, where kernels record
+// bounded-wait failures (cached per device; nullptr if it cannot be had).
+unsigned *device_status();
+
+// Launch the bounded-wait self-test kernel (see dan_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
+
 } // namespace dan

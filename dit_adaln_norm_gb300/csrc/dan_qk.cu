@@ -8,8 +8,9 @@
 // buffers; inputs are zero-copy row-strided views of the packed QKV GEMM
 // output (section 4).
 //
-// Work unit = (token, Q|K|V, group of up to 24 heads), one warp each,
-// grid-stride over units.  A half-warp covers one head: lane l (0..15) owns the 16-byte fragment of
+// Work unit = (token, Q|K|V, group of up to 24 heads): one bulk copy into
+// a shared-memory ring slot, processed by one consumer warp (see
+// dan_ring.cuh for the ring).  A half-warp covers one head: lane l (0..15) owns the 16-byte fragment of
 // columns 8l..8l+7, so each head is one coalesced 256-byte load/store and
 // the two halves of a warp take adjacent heads (512 contiguous bytes).  The
 // per-token RoPE row and the stream's weight fragment are read once per unit.
@@ -18,6 +19,7 @@
 // recursive-halving fold so that each lane ends with one head's sum.
 #include "dan_device.cuh"
 #include "dan_internal.h"
+#include "dan_ring.cuh"
 
 namespace dan {
 
@@ -32,9 +34,12 @@ struct QkParams {
     uint4 *q_out, *k_out, *v_out;
     int H;
     int groups; // head groups of kGroup heads per (token, kind)
+    unsigned *status;
+    unsigned long long limit_ns;
 };
 
-constexpr int kQkWarps = 12;
+constexpr int kQkNC = 8;  // consumer warps per CTA
+constexpr int kQkSPC = 2; // ring slots per consumer
 constexpr int kHeadsPerLane = 12;           // heads a half-warp lane holds per unit
 constexpr int kGroup = 2 * kHeadsPerLane;   // heads per unit
 
@@ -49,22 +54,43 @@ struct QkUnit {
     int kind, h0, s;
 };
 
-__device__ __forceinline__ void qk_load(QkUnit &U, const QkParams &p, int64_t u, int half, int fl)
+// Unit k of a CTA whose tokens start at t0: token t0 + k / (3 * groups),
+// then Q, K, V, each split in head groups.
+__device__ __forceinline__ void qk_unit(QkUnit &U, const QkParams &p, int64_t t0, int k)
 {
-    const int64_t tg = u / 3;
-    U.kind = (int)(u - 3 * tg);
-    U.tok = tg / p.groups;
-    U.h0 = (int)(tg - U.tok * p.groups) * kGroup;
+    const int per_tok = 3 * p.groups;
+    U.tok = t0 + k / per_tok;
+    const int rem = k % per_tok;
+    U.kind = rem / p.groups;
+    U.h0 = (rem % p.groups) * kGroup;
     U.s = U.tok < p.T0 ? 0 : 1;
+}
+
+__device__ __forceinline__ const uint4 *qk_src(const QkUnit &U, const QkParams &p)
+{
     const int64_t t = U.s ? U.tok - p.T0 : U.tok;
-    const uint4 *src =
-        (U.kind == 0 ? p.q[U.s] : U.kind == 1 ? p.k[U.s] : p.v[U.s]) + t * p.stride8[U.s];
+    return (U.kind == 0 ? p.q[U.s] : U.kind == 1 ? p.k[U.s] : p.v[U.s]) + t * p.stride8[U.s] +
+           U.h0 * 16;
+}
+
+__device__ __forceinline__ int qk_heads(const QkUnit &U, const QkParams &p)
+{
+    return p.H - U.h0 < kGroup ? p.H - U.h0 : kGroup;
+}
+
+// Copy the unit's heads from its ring slot into registers, and read the
+// stream's weight fragment and the token's cos/sin for Q and K.
+__device__ __forceinline__ void qk_take(QkUnit &U, const QkParams &p, const uint4 *slot, int half,
+                                        int fl)
+{
+    const int nh = qk_heads(U, p);
 #pragma unroll
     for (int k = 0; k < kHeadsPerLane; ++k) {
-        const int h = U.h0 + half + 2 * k;
-        U.x[k] = h < p.H ? ld_stream(src + h * 16 + fl) : make_uint4(0, 0, 0, 0);
+        const int hh = half + 2 * k;
+        U.x[k] = hh < nh ? slot[hh * 16 + fl] : make_uint4(0, 0, 0, 0);
     }
     if (U.kind != 2) {
+        const int64_t t = U.s ? U.tok - p.T0 : U.tok;
         U.w = ld_vec((U.kind == 0 ? p.wq[U.s] : p.wk[U.s]) + fl);
         U.c4 = ld_vec(p.rope[U.s] + t * 32 + fl);      // cos of pairs 4fl..4fl+3
         U.s4 = ld_vec(p.rope[U.s] + t * 32 + 16 + fl); // sin of the same pairs
@@ -150,27 +176,60 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
     }
 }
 
-// Warps walk units u = global warp, + total warps, ...; two register
-// buffers alternate so each warp has its next unit's loads in flight.
-__global__ void __launch_bounds__(kQkWarps * 32, 1) qk_norm_rope_kernel(const QkParams p)
+// CTA c takes the contiguous tokens [c*T/G, (c+1)*T/G) and streams their
+// units through a ring of 6 KB slots (dan_ring.cuh): warp 0 lane 0 issues
+// one bulk copy per unit, warps 1..kQkNC consume.
+__global__ void __launch_bounds__(32 * (kQkNC + 1), 1) qk_norm_rope_kernel(const QkParams p)
 {
-    const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, fl = lane & 15;
-    const int64_t nwarps = (int64_t)gridDim.x * kQkWarps;
-    const int64_t units = 3 * p.T_all * p.groups;
+    using R = RingSchedule<kQkNC, kQkSPC>;
+    constexpr int kSlot = kGroup * 16; // uint4 per slot
+    extern __shared__ __align__(128) uint4 smem[];
+    uint4 *ring = smem;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + R::S * kSlot);
+    uint64_t *empty = full + R::S;
 
-    QkUnit A, B;
-    int64_t ua = (int64_t)blockIdx.x * kQkWarps + (threadIdx.x >> 5), ub = ua + nwarps;
-    if (ua < units) qk_load(A, p, ua, half, fl);
-    if (ub < units) qk_load(B, p, ub, half, fl);
-    while (ua < units) {
-        qk_process(A, p, half, fl);
-        ua = ub + nwarps;
-        if (ua < units) qk_load(A, p, ua, half, fl);
-        if (ub >= units) break;
-        qk_process(B, p, half, fl);
-        ub = ua + nwarps;
-        if (ub < units) qk_load(B, p, ub, half, fl);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = (lane >> 4) & 1, fl = lane & 15;
+    const int64_t G = gridDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * p.T_all / G;
+    const int64_t t1 = (int64_t)(blockIdx.x + 1) * p.T_all / G;
+    const int n = (int)((t1 - t0) * 3 * p.groups);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < R::S; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0)
+            ring_produce<kQkNC, kQkSPC>(n, full, empty, p.status, p.limit_ns, [&](int k, int s) {
+                QkUnit U;
+                qk_unit(U, p, t0, k);
+                const unsigned bytes = (unsigned)qk_heads(U, p) * 256u;
+                mbar_arrive_expect_tx(full + s, bytes);
+                bulk_load(ring + s * kSlot, qk_src(U, p), bytes, full + s);
+            });
+        return;
+    }
+
+    const int c = warp - 1;
+    for (int i = 0;; ++i) {
+        const int k = c + i * kQkNC;
+        if (k >= n) break;
+        const int s = R::slot(c, i);
+        if (!mbar_wait(full + s, R::phase(i), p.limit_ns)) {
+            set_status(p.status, kStatusWaitFull);
+            return;
+        }
+        QkUnit U;
+        qk_unit(U, p, t0, k);
+        qk_take(U, p, ring + s * kSlot, half, fl);
+        ring_release(empty + s, lane);
+        qk_process(U, p, half, fl);
     }
 }
 
@@ -194,21 +253,20 @@ cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &q, cudaStream_t s)
     p.v_out = static_cast<uint4 *>(q.v_out);
     p.H = (int)q.heads;
     p.groups = (int)((q.heads + kGroup - 1) / kGroup);
+    p.status = device_status();
+    p.limit_ns = 1000000000ull;
 
-    static int per_sm = 0; // resident CTAs per SM (a property of the kernel build)
-    if (per_sm == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel, kQkWarps * 32,
-                                                          0) != cudaSuccess ||
-            n < 1)
-            n = 1;
-        per_sm = n;
+    constexpr int S = kQkNC * kQkSPC;
+    const int smem = S * kGroup * 256 + 2 * S * 8;
+    static bool configured = false; // dynamic shared memory above 48 KB (once)
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
     }
-    const int64_t units = 3 * p.T_all * p.groups;
-    const int64_t want = (units + kQkWarps - 1) / kQkWarps;
-    const int64_t cap = (int64_t)sm_count() * per_sm;
-    const int grid = (int)(want < cap ? want : cap);
-    qk_norm_rope_kernel<<<grid, kQkWarps * 32, 0, s>>>(p);
+    const int grid = (int)(p.T_all < sm_count() ? p.T_all : sm_count());
+    qk_norm_rope_kernel<<<grid, 32 * (kQkNC + 1), smem, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -60,6 +60,10 @@ def load():
             fn.restype = ctypes.c_int
         lib.dan_status_string.argtypes = [ctypes.c_int]
         lib.dan_status_string.restype = ctypes.c_char_p
+        lib.dan_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.dan_get_device_status.restype = ctypes.c_int
+        lib.dan_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _P]
+        lib.dan_selftest_wait_timeout.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -72,6 +76,20 @@ def declared_symbols() -> list[str]:
 
 def status_string(status: int) -> str:
     return load().dan_status_string(int(status)).decode()
+
+
+def device_status() -> int:
+    """Read and clear the current device's status word (bit 1: a consumer
+    gave up waiting for a row, 2: the producer for a slot, 4: the producer
+    for its own copies).  Synchronous; 0 when every wait completed."""
+    v = ctypes.c_uint(0)
+    _check(load().dan_get_device_status(ctypes.byref(v)), "dan_get_device_status")
+    return v.value
+
+
+def selftest_wait_timeout(limit_ns: int):
+    """Launch the bounded-wait self-test on the current stream."""
+    _check(load().dan_selftest_wait_timeout(int(limit_ns), _stream()), "dan_selftest_wait_timeout")
 
 
 def _stream() -> int:

@@ -77,6 +77,26 @@ typedef enum {
 /* Human-readable name of a status code (static string, never NULL). */
 const char *dan_status_string(int status);
 
+/* ------------------------------------------------------ device status
+ * The kernels stream rows through shared memory with bulk copies whose
+ * completion they wait for on mbarriers.  Every such wait is bounded (about
+ * one second); a wait that runs out makes the kernel record a bit in the
+ * current device's status word and return, leaving its outputs incomplete:
+ *   1 = a consumer gave up on a row, 2 = the producer gave up on a slot,
+ *   4 = the producer gave up waiting for its own copies.
+ * dan_get_device_status reads the word of the current device into *status
+ * and clears it.  It is synchronous: call it after synchronising the streams
+ * the kernels ran on.  Returns DAN_OK, DAN_EINVAL (status NULL) or DAN_ECUDA.
+ * The word is static device memory of the library: nothing is allocated. */
+int dan_get_device_status(unsigned int *status);
+
+/* Self-test of the bounded wait: launches one warp that waits on an
+ * mbarrier nothing completes, for limit_ns nanoseconds (1 .. 2e9), then
+ * records status bit 1 and returns.  Lets a test check that a wait that
+ * runs out reports through dan_get_device_status and leaves the context
+ * usable.  Asynchronous on `stream`. */
+int dan_selftest_wait_timeout(unsigned long long limit_ns, void *stream);
+
 /* ------------------------------------------------------------------ RMS
  * y[b,t,:] = bf16(bf16(n * o) + shift) per element, where
  *   n = bf16(rn(x * rstd))             (weight == NULL)

@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = ops.declared_symbols()
-    assert len(names) == 9
+    assert len(names) == 11
     for n in names:
         assert hasattr(lib, n), n
 
@@ -125,3 +125,10 @@ def test_binding_raises_without_cuda_tensors():
         ops.rms_modulate(torch.zeros(1, 2, 2048, dtype=torch.bfloat16),
                          torch.zeros(1, 2048, dtype=torch.bfloat16),
                          torch.zeros(1, 2048, dtype=torch.bfloat16), 1e-6)
+
+
+def test_selftest_argument_checks(lib):
+    # invalid limits are rejected before any CUDA call
+    assert lib.dan_selftest_wait_timeout(0, None) == EINVAL
+    assert lib.dan_selftest_wait_timeout(3_000_000_000, None) == EINVAL
+    assert lib.dan_get_device_status(None) == EINVAL
