@@ -137,18 +137,21 @@ struct RingSchedule {
 // Producer side for `n` rows: row k belongs to consumer k % NC as its
 // (k / NC)-th row.  `issue(k, slot)` must arm and issue the copies of row k
 // into `slot` (one mbar_arrive_expect_tx on full[slot] with the total bytes,
-// then the bulk copies).  Returns after the last copy of every slot landed.
+// then the bulk copies).  Returns after the last copy of every slot landed,
+// with the status bits it set (0 when every wait completed).
 template <int NC, int SPC, typename Issue>
-__device__ __forceinline__ void ring_produce(int n, uint64_t *full, uint64_t *empty,
-                                             unsigned *status, unsigned long long limit_ns,
-                                             Issue issue)
+__device__ __forceinline__ unsigned ring_produce(int n, uint64_t *full, uint64_t *empty,
+                                                 unsigned *status, unsigned long long limit_ns,
+                                                 Issue issue)
 {
     using R = RingSchedule<NC, SPC>;
+    unsigned failed = 0;
     int issued = 0;
     for (int k = 0; k < n; ++k) {
         const int c = k % NC, i = k / NC, s = R::slot(c, i);
         if (i >= SPC && !mbar_wait(empty + s, R::phase(i - SPC), limit_ns)) {
             set_status(status, kStatusWaitEmpty);
+            failed |= kStatusWaitEmpty;
             break;
         }
         issue(k, s);
@@ -160,9 +163,11 @@ __device__ __forceinline__ void ring_produce(int n, uint64_t *full, uint64_t *em
         const int c = k % NC, i = k / NC;
         if (!mbar_wait(full + R::slot(c, i), R::phase(i), limit_ns)) {
             set_status(status, kStatusWaitDrain);
+            failed |= kStatusWaitDrain;
             break;
         }
     }
+    return failed;
 }
 
 } // namespace dan

@@ -63,6 +63,7 @@ struct RowParams {
     float eps;
     unsigned *status;            // device status word (bounded-wait failures)
     unsigned long long limit_ns; // bound of every wait
+    unsigned *cta_status;        // per-CTA failure records (CTA_STATUS kernels only)
 };
 
 // Per-batch vector fragment f: which = 0 -> bf16(1 + scale), 1 -> shift,
@@ -416,7 +417,10 @@ struct RowShape {
 // CTA c takes the contiguous rows [c*R/G, (c+1)*R/G).  Warp 0 lane 0 is
 // the producer; warps 1..NC are consumers (one row at a time, the whole
 // row in registers: LW logical warps per lane for RMS, 4 for LayerNorm).
-template <int KIND, int LW, int FPT, int NC, int SPC, bool HAS_W, bool RAGGED, bool STAGED>
+// CTA_STATUS kernels also keep one failure record per CTA in
+// p.cta_status[blockIdx.x], cleared when the CTA starts.
+template <int KIND, int LW, int FPT, int NC, int SPC, bool HAS_W, bool RAGGED, bool STAGED,
+          bool CTA_STATUS = false>
 __global__ void __launch_bounds__(32 * (NC + 1), 1)
     row_ring_kernel(const RowParams p, const InvTable2 inv)
 {
@@ -439,6 +443,7 @@ __global__ void __launch_bounds__(32 * (NC + 1), 1)
     const int n = (int)((int64_t)(blockIdx.x + 1) * p.rows / G - r0);
 
     if (threadIdx.x == 0) {
+        if (CTA_STATUS) p.cta_status[blockIdx.x] = 0u;
         for (int s = 0; s < R::S; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
@@ -463,10 +468,13 @@ __global__ void __launch_bounds__(32 * (NC + 1), 1)
     stage_end<NV>(p, s_vec);
 
     if (warp == 0) {
-        if (producer)
-            ring_produce<NC, SPC>(n, full, empty, p.status, p.limit_ns, [&](int k, int s) {
-                if (k >= R::S) issue(k, s); // the first S rows were issued above
-            });
+        if (producer) {
+            const unsigned failed =
+                ring_produce<NC, SPC>(n, full, empty, p.status, p.limit_ns, [&](int k, int s) {
+                    if (k >= R::S) issue(k, s); // the first S rows were issued above
+                });
+            if (CTA_STATUS && failed) set_status(p.cta_status + blockIdx.x, failed);
+        }
         return;
     }
 
@@ -477,6 +485,7 @@ __global__ void __launch_bounds__(32 * (NC + 1), 1)
         const int s = R::slot(c, i);
         if (!mbar_wait(full + s, R::phase(i), p.limit_ns)) {
             set_status(p.status, kStatusWaitFull);
+            if (CTA_STATUS) set_status(p.cta_status + blockIdx.x, kStatusWaitFull);
             return;
         }
         const uint4 *src = ring + (int64_t)s * NIN * F;
@@ -581,6 +590,7 @@ RowParams make_params(const RowProblem &q)
     p.Bs = 0;
     p.status = device_status();
     p.limit_ns = kWaitLimitNs;
+    p.cta_status = nullptr;
     return p;
 }
 

@@ -27,6 +27,7 @@ _I = ctypes.c_int64
 _F = ctypes.c_float
 _SIGS = {
     "dan_rms_modulate": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P],
+    "dan_rms_modulate_noalloc": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P],
     "dan_can_use_rms_modulate": [_P, _P, _P, _P, _I, _P, _I, _I, _I, _F],
     "dan_gated_rms_modulate": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F, _P],
     "dan_can_use_gated_rms_modulate": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F],

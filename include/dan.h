@@ -118,6 +118,25 @@ int dan_can_use_rms_modulate(const dan_bf16 *x, const dan_bf16 *weight, const da
                              const dan_bf16 *shift, int64_t vec_bstride, const dan_bf16 *y,
                              int64_t B, int64_t T, int64_t D, float eps);
 
+/* RMS + modulate for callers that cannot allocate device memory: code that
+ * runs inside a stream capture whose mode forbids allocation calls, or a
+ * runtime whose device memory belongs to an allocator of its own (a caching
+ * pool that must not see foreign cudaMalloc/cudaFree).  The pages have no
+ * counterpart; it is the same kernel and result as dan_rms_modulate (same
+ * arguments, validation and output bits).  Its scratch -- one bounded-wait
+ * failure record per CTA, in addition to the device status word -- lives in
+ * a static device array of 256 records (1 KB) that the library holds on
+ * every GPU that loads it until the process exits; no device memory is
+ * allocated or freed.  The launch uses one CTA per SM (at most the row
+ * count); a GPU with more than 256 SMs gets DAN_EUNSUPPORTED.  The first
+ * call on a device looks up the array's address (cudaGetSymbolAddress), so
+ * make that first call before any stream capture.  Every call shares the
+ * array and each CTA clears its record when it starts: calls that overlap
+ * on the GPU race on it. */
+int dan_rms_modulate_noalloc(const dan_bf16 *x, const dan_bf16 *weight, const dan_bf16 *scale,
+                             const dan_bf16 *shift, int64_t vec_bstride, dan_bf16 *y, int64_t B,
+                             int64_t T, int64_t D, float eps, void *stream);
+
 /* ------------------------------------------------------------- gated RMS
  * r_out = bf16(rn(r + bf16(rn(gate * h)))) (the updated residual stream),
  * then y = the RMS row above applied to r_out.  gate, scale, shift share
