@@ -9,6 +9,9 @@
 
 #include <cmath>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
 
 namespace {
 
@@ -214,6 +217,48 @@ int sm_count()
         cache[slot] = n;
     }
     return cache[slot];
+}
+
+int max_smem_optin()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    int &c = cache[dev & 63];
+    if (c == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            v <= 0)
+            v = 48 * 1024;
+        c = v;
+    }
+    return c;
+}
+
+cudaError_t allow_dynamic_smem(const void *fn, int smem)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> done; // (kernel, device) -> bytes set
+    int dev = 0;
+    const cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess) return ge;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find({fn, dev});
+    if (it == done.end()) {
+        // Every kernel asks for the largest shared-memory split of the SM's
+        // on-chip memory, so consecutive launches of different kernels never
+        // wait for the SM to change its L1 / shared split.
+        const cudaError_t e = cudaFuncSetAttribute(
+            fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        it = done.emplace(std::make_pair(fn, dev), 0).first;
+    }
+    if (smem > 48 * 1024 && it->second < smem) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        it->second = smem;
+    }
+    return cudaSuccess;
 }
 
 } // namespace dan

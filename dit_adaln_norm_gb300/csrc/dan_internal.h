@@ -33,6 +33,28 @@ struct QkProblem {
     int64_t heads;
 };
 
+// Launch fn<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialization: the grid may be scheduled before the previous grid in the
+// stream has finished, so its kernel must begin with grid_dependency_wait()
+// (dan_ring.cuh).  This hides the launch and the prologue behind the tail of
+// the previous kernel; the order of memory accesses is unchanged.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*fn)(KArgs...), int grid, int block, int smem, cudaStream_t s,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 cudaError_t launch_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_gated_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_ln_modulate(const RowProblem &p, cudaStream_t s);
@@ -40,6 +62,14 @@ cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &p, cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Largest dynamic shared memory a block may opt in to on the current device.
+int max_smem_optin();
+
+// Let kernel `fn` use `smem` bytes of dynamic shared memory on the current
+// device, and prefer the largest shared-memory carveout (each attribute set
+// once per kernel and device, thread-safe).
+cudaError_t allow_dynamic_smem(const void *fn, int smem);
 
 // Device address of the current device's status word, where kernels record
 // bounded-wait failures (cached per device; nullptr if it cannot be had).

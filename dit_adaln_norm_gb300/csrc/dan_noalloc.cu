@@ -32,32 +32,6 @@ unsigned *noalloc_scratch()
     return c;
 }
 
-template <int LW, int NC, int SPC>
-cudaError_t launch_noalloc(const RowProblem &q, unsigned *scratch, int grid, cudaStream_t s)
-{
-    constexpr int S = NC * SPC;
-    RowParams p = make_params(q);
-    p.cta_status = scratch;
-    const int64_t row_bytes = q.D * 2;
-    const int64_t fixed = (int64_t)S * row_bytes + (q.weight ? row_bytes : 0) + 2 * S * 8;
-    const int64_t vec_bytes = q.B * 2 * row_bytes;
-    const int64_t room = (int64_t)max_smem_optin() - fixed;
-    p.Bs = (vec_bytes <= kStageBudget && vec_bytes <= room) ? (int)q.B : 0;
-    const int smem = (int)(fixed + (p.Bs ? vec_bytes : 0));
-    const InvTable2 inv = inv_table();
-    auto go = [&](auto fn) -> cudaError_t {
-        const cudaError_t e = allow_smem(fn, smem);
-        if (e != cudaSuccess) return e;
-        fn<<<grid, 32 * (NC + 1), smem, s>>>(p, inv);
-        return cudaGetLastError();
-    };
-    if (q.weight)
-        return p.Bs ? go(row_ring_kernel<kRms, LW, 8, NC, SPC, true, false, true, true>)
-                    : go(row_ring_kernel<kRms, LW, 8, NC, SPC, true, false, false, true>);
-    return p.Bs ? go(row_ring_kernel<kRms, LW, 8, NC, SPC, false, false, true, true>)
-                : go(row_ring_kernel<kRms, LW, 8, NC, SPC, false, false, false, true>);
-}
-
 } // namespace
 } // namespace dan
 
@@ -78,10 +52,11 @@ extern "C" int dan_rms_modulate_noalloc(const dan_bf16 *x, const dan_bf16 *weigh
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (D) {
-    case 2048: e = dan::launch_noalloc<1, 8, 1>(q, scratch, grid, s); break;
-    case 4096: e = dan::launch_noalloc<2, 8, 1>(q, scratch, grid, s); break;
-    case 6144: e = dan::launch_noalloc<3, 4, 2>(q, scratch, grid, s); break;
-    default: e = dan::launch_noalloc<4, 4, 2>(q, scratch, grid, s); break; // 8192
+    // the shapes of dan_rms_modulate, with a failure record per CTA
+    case 2048: e = dan::launch_ring<dan::kRms, 1, 8, 8, 2, false, true>(q, s, scratch); break;
+    case 4096: e = dan::launch_ring<dan::kRms, 2, 8, 8, 2, false, true>(q, s, scratch); break;
+    case 6144: e = dan::launch_ring<dan::kRms, 3, 8, 8, 1, false, true>(q, s, scratch); break;
+    default: e = dan::launch_ring<dan::kRms, 4, 8, 8, 1, false, true>(q, s, scratch); break;
     }
     return e == cudaSuccess ? DAN_OK : DAN_ECUDA;
 }

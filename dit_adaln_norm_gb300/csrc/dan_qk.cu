@@ -38,10 +38,14 @@ struct QkParams {
     unsigned long long limit_ns;
 };
 
-constexpr int kQkNC = 8;  // consumer warps per CTA
-constexpr int kQkSPC = 2; // ring slots per consumer
-constexpr int kHeadsPerLane = 12;           // heads a half-warp lane holds per unit
-constexpr int kGroup = 2 * kHeadsPerLane;   // heads per unit
+constexpr int kQkNW = 8;  // warps per CTA (measured best among 4..16)
+constexpr int kQkSPC = 1; // slots per warp
+constexpr int kHeadsPerLane = 12;         // heads a half-warp lane holds per unit
+constexpr int kGroup = 2 * kHeadsPerLane; // heads per unit
+// A ring slot holds one unit's heads (16 fragments each) and, for Q and K,
+// the token's cos/sin row (128 fp32 = 32 fragments) behind them.
+constexpr int kSlotRope = kGroup * 16;
+constexpr int kSlot = kSlotRope + 32;
 
 // One unit of work = (token, Q|K|V, group of up to kGroup heads), as
 // loaded registers: the head fragments plus, for Q and K, the weight
@@ -78,10 +82,17 @@ __device__ __forceinline__ int qk_heads(const QkUnit &U, const QkParams &p)
     return p.H - U.h0 < kGroup ? p.H - U.h0 : kGroup;
 }
 
-// Copy the unit's heads from its ring slot into registers, and read the
-// stream's weight fragment and the token's cos/sin for Q and K.
-__device__ __forceinline__ void qk_take(QkUnit &U, const QkParams &p, const uint4 *slot, int half,
-                                        int fl)
+__device__ __forceinline__ const float4 *qk_rope_row(const QkUnit &U, const QkParams &p)
+{
+    const int64_t t = U.s ? U.tok - p.T0 : U.tok;
+    return p.rope[U.s] + t * 32;
+}
+
+// Copy the unit's heads from its ring slot into registers, with, for Q and
+// K, the stream's weight fragment (staged in s_w: wq_txt, wk_txt, wq_img,
+// wk_img) and the token's cos/sin for this lane's four pairs (in the slot).
+__device__ __forceinline__ void qk_take(QkUnit &U, const QkParams &p, const uint4 *slot,
+                                        const uint4 *s_w, int half, int fl)
 {
     const int nh = qk_heads(U, p);
 #pragma unroll
@@ -90,10 +101,10 @@ __device__ __forceinline__ void qk_take(QkUnit &U, const QkParams &p, const uint
         U.x[k] = hh < nh ? slot[hh * 16 + fl] : make_uint4(0, 0, 0, 0);
     }
     if (U.kind != 2) {
-        const int64_t t = U.s ? U.tok - p.T0 : U.tok;
-        U.w = ld_vec((U.kind == 0 ? p.wq[U.s] : p.wk[U.s]) + fl);
-        U.c4 = ld_vec(p.rope[U.s] + t * 32 + fl);      // cos of pairs 4fl..4fl+3
-        U.s4 = ld_vec(p.rope[U.s] + t * 32 + 16 + fl); // sin of the same pairs
+        U.w = s_w[(2 * U.s + U.kind) * 16 + fl];
+        const float4 *rope = reinterpret_cast<const float4 *>(slot + kSlotRope);
+        U.c4 = rope[fl];      // cos of pairs 4fl..4fl+3
+        U.s4 = rope[16 + fl]; // sin of the same pairs
     }
 }
 
@@ -176,17 +187,18 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
     }
 }
 
-// CTA c takes the contiguous tokens [c*T/G, (c+1)*T/G) and streams their
-// units through a ring of 6 KB slots (dan_ring.cuh): warp 0 lane 0 issues
-// one bulk copy per unit, warps 1..kQkNC consume.
-__global__ void __launch_bounds__(32 * (kQkNC + 1), 1) qk_norm_rope_kernel(const QkParams p)
+// CTA c takes the contiguous tokens [c*T/G, (c+1)*T/G); its warp w takes
+// the CTA's units w, w + kQkNW, ... and requests each kQkSPC units ahead
+// into its own 6.5 KB slots (dan_ring.cuh): one bulk copy of the unit's
+// heads, plus one of the token's cos/sin row for Q and K.  The four
+// 256-byte weight vectors are staged in shared memory once per CTA.
+__global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkParams p)
 {
-    using R = RingSchedule<kQkNC, kQkSPC>;
-    constexpr int kSlot = kGroup * 16; // uint4 per slot
+    using Pipe = WarpPipe<kQkSPC>;
     extern __shared__ __align__(128) uint4 smem[];
     uint4 *ring = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + R::S * kSlot);
-    uint64_t *empty = full + R::S;
+    uint4 *s_w = ring + kQkNW * kQkSPC * kSlot; // 4 x 16 fragments
+    uint64_t *full = reinterpret_cast<uint64_t *>(s_w + 64);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = (lane >> 4) & 1, fl = lane & 15;
@@ -196,39 +208,49 @@ __global__ void __launch_bounds__(32 * (kQkNC + 1), 1) qk_norm_rope_kernel(const
     const int n = (int)((t1 - t0) * 3 * p.groups);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < R::S; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
-        }
+        for (int s = 0; s < kQkNW * kQkSPC; ++s) mbar_init(full + s, 1);
         mbar_init_fence();
     }
-    __syncthreads();
-
-    if (warp == 0) {
-        if (lane == 0)
-            ring_produce<kQkNC, kQkSPC>(n, full, empty, p.status, p.limit_ns, [&](int k, int s) {
-                QkUnit U;
-                qk_unit(U, p, t0, k);
-                const unsigned bytes = (unsigned)qk_heads(U, p) * 256u;
-                mbar_arrive_expect_tx(full + s, bytes);
-                bulk_load(ring + s * kSlot, qk_src(U, p), bytes, full + s);
-            });
-        return;
+    grid_dependency_wait(); // no global access above this line
+    allow_dependents();
+    if (threadIdx.x < 64) { // the weights of a stream with no tokens are never read
+        const int v = threadIdx.x >> 4, s = v >> 1;
+        if (s == 0 ? p.T0 > 0 : p.T_all > p.T0)
+            s_w[threadIdx.x] = ld_vec((v & 1 ? p.wk[s] : p.wq[s]) + (threadIdx.x & 15));
     }
+    __syncthreads(); // barriers initialised, weights staged
 
-    const int c = warp - 1;
-    for (int i = 0;; ++i) {
-        const int k = c + i * kQkNC;
-        if (k >= n) break;
-        const int s = R::slot(c, i);
-        if (!mbar_wait(full + s, R::phase(i), p.limit_ns)) {
-            set_status(p.status, kStatusWaitFull);
+    uint4 *slots = ring + warp * kQkSPC * kSlot;
+    uint64_t *bar = full + warp * kQkSPC;
+    const int units = warp < n ? (n - warp + kQkNW - 1) / kQkNW : 0;
+    auto request = [&](int i) { // lane 0 only
+        QkUnit U;
+        qk_unit(U, p, t0, warp + kQkNW * i);
+        const unsigned bytes = (unsigned)qk_heads(U, p) * 256u;
+        uint4 *slot = slots + Pipe::slot(i) * kSlot;
+        uint64_t *b = bar + Pipe::slot(i);
+        if (U.kind == 2) {
+            mbar_arrive_expect_tx(b, bytes);
+            bulk_load(slot, qk_src(U, p), bytes, b);
+        } else {
+            mbar_arrive_expect_tx(b, bytes + 512u);
+            bulk_load(slot, qk_src(U, p), bytes, b);
+            bulk_load(slot + kSlotRope, qk_rope_row(U, p), 512u, b);
+        }
+    };
+    if (lane == 0)
+        for (int i = 0; i < kQkSPC && i < units; ++i) request(i);
+
+    for (int i = 0; i < units; ++i) {
+        if (!Pipe::wait(bar, i, p.limit_ns)) {
+            Pipe::abort(bar, i, units, p.status, p.limit_ns);
             return;
         }
         QkUnit U;
-        qk_unit(U, p, t0, k);
-        qk_take(U, p, ring + s * kSlot, half, fl);
-        ring_release(empty + s, lane);
+        qk_unit(U, p, t0, warp + kQkNW * i);
+        qk_take(U, p, slots + Pipe::slot(i) * kSlot, s_w, half, fl);
+        slot_reads_done();
+        if (lane == 0 && i + kQkSPC < units) request(i + kQkSPC);
         qk_process(U, p, half, fl);
     }
 }
@@ -256,18 +278,12 @@ cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &q, cudaStream_t s)
     p.status = device_status();
     p.limit_ns = 1000000000ull;
 
-    constexpr int S = kQkNC * kQkSPC;
-    const int smem = S * kGroup * 256 + 2 * S * 8;
-    static bool configured = false; // dynamic shared memory above 48 KB (once)
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            qk_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    constexpr int S = kQkNW * kQkSPC;
+    const int smem = S * kSlot * 16 + 64 * 16 + S * 8;
+    const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(qk_norm_rope_kernel), smem);
+    if (e != cudaSuccess) return e;
     const int grid = (int)(p.T_all < sm_count() ? p.T_all : sm_count());
-    qk_norm_rope_kernel<<<grid, 32 * (kQkNC + 1), smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(qk_norm_rope_kernel, grid, 32 * kQkNW, smem, s, p);
 }
 
 } // namespace dan

@@ -1,19 +1,17 @@
-// dan_ring.cuh -- TMA bulk-copy row ring: mbarrier and cp.async.bulk
+// dan_ring.cuh -- warp-fed bulk-copy pipelines: mbarrier and cp.async.bulk
 // primitives, the bounded wait, and the slot schedule shared by the kernels.
 //
-// One producer thread per CTA issues 1-D bulk copies (cp.async.bulk, global
-// -> shared, completion counted in bytes on an mbarrier) of whole rows into
-// a ring of shared-memory slots, in row order, so rows land roughly in the
-// order they are consumed; consumer warps take rows from the ring.
-//
-// Slot ownership: consumer warp c owns slots c, c + NC, ..., c + NC*(SPC-1)
-// and takes the CTA's rows c, c + NC, c + 2NC, ...; its i-th row lives in
-// slot c + NC*(i % SPC) in phase (i / SPC) & 1.  A slot is therefore only
-// ever used by one consumer, which consumed its previous phase itself: a
-// barrier is never two phases behind its waiter, so the parity test cannot
-// alias.  The producer refills a slot only after its consumer released it,
-// so each slot has at most one copy in flight; before the CTA exits the
-// producer waits for the last copy it issued into every slot.
+// Every warp of a CTA requests its own work units (whole rows, or a head
+// group of one token) with 1-D bulk copies (cp.async.bulk, global ->
+// shared, completion counted in bytes on an mbarrier) into SPC shared-memory
+// slots that it alone uses.  Its i-th unit goes to slot i % SPC and
+// completes phase (i / SPC) & 1 of that slot's barrier.  As soon as the
+// warp has copied unit i out of its slot into registers it requests unit
+// i + SPC into the same slot, so the copy overlaps its work on unit i.
+// Nothing else waits on a warp's barriers and the warp waits on them in
+// order, so a barrier is never more than one phase ahead of its waiter and
+// the parity test cannot alias; no copy is left in flight when the warp
+// finishes, because every unit it requests is one it then waits for.
 //
 // Every wait is bounded in time.  After the limit the waiter sets a bit in a
 // device status word and returns; the host reads it with
@@ -26,9 +24,8 @@
 namespace dan {
 
 // Status bits a kernel may set in the device status word.
-constexpr unsigned kStatusWaitFull = 1u;  // a consumer gave up waiting for a row
-constexpr unsigned kStatusWaitEmpty = 2u; // the producer gave up waiting for a slot
-constexpr unsigned kStatusWaitDrain = 4u; // the producer gave up waiting for its own copies
+constexpr unsigned kStatusWaitFull = 1u;  // a warp gave up waiting for a unit it requested
+constexpr unsigned kStatusWaitDrain = 4u; // after that, it gave up waiting for its other copies
 
 __device__ __forceinline__ unsigned smem_addr(const void *p)
 {
@@ -60,11 +57,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
@@ -109,16 +101,31 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
                  : "memory");
 }
 
-// A consumer's release of a slot: its generic-proxy reads of the slot must
-// be ordered before the producer's next bulk copy (async proxy) into it,
-// which needs a proxy fence by every reading thread before the arrive
-// (measured: without it a refill occasionally overwrote a slot still being
-// read).  All 32 lanes must call this.
-__device__ __forceinline__ void ring_release(uint64_t *empty_slot, int lane)
+// After a warp's generic-proxy reads of a slot, order them before the next
+// bulk copy (async proxy) into it: every reading lane fences, then the warp
+// converges, and lane 0 may issue the refill (measured: without the fence a
+// refill occasionally overwrote a slot still being read).  All 32 lanes
+// must call this.
+__device__ __forceinline__ void slot_reads_done()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty_slot);
+}
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization (launch_overlapped) may start while the grid before it in
+// the stream is still running; every thread calls grid_dependency_wait()
+// before its first global-memory access, which returns once that grid has
+// completed and its writes are visible (at once when there is none).
+// allow_dependents() lets the next such grid start the same way.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void set_status(unsigned *status, unsigned bit)
@@ -126,48 +133,34 @@ __device__ __forceinline__ void set_status(unsigned *status, unsigned bit)
     if (status) atomicOr(status, bit);
 }
 
-// Slot and phase of the i-th row of consumer c (see the header comment).
-template <int NC, int SPC>
-struct RingSchedule {
-    static constexpr int S = NC * SPC;
-    __device__ __forceinline__ static int slot(int c, int i) { return c + NC * (i % SPC); }
+// Slot and barrier phase of a warp's i-th unit (see the header comment).
+template <int SPC>
+struct WarpPipe {
+    __device__ __forceinline__ static int slot(int i) { return i % SPC; }
     __device__ __forceinline__ static unsigned phase(int i) { return (unsigned)(i / SPC) & 1u; }
-};
 
-// Producer side for `n` rows: row k belongs to consumer k % NC as its
-// (k / NC)-th row.  `issue(k, slot)` must arm and issue the copies of row k
-// into `slot` (one mbar_arrive_expect_tx on full[slot] with the total bytes,
-// then the bulk copies).  Returns after the last copy of every slot landed,
-// with the status bits it set (0 when every wait completed).
-template <int NC, int SPC, typename Issue>
-__device__ __forceinline__ unsigned ring_produce(int n, uint64_t *full, uint64_t *empty,
-                                                 unsigned *status, unsigned long long limit_ns,
-                                                 Issue issue)
-{
-    using R = RingSchedule<NC, SPC>;
-    unsigned failed = 0;
-    int issued = 0;
-    for (int k = 0; k < n; ++k) {
-        const int c = k % NC, i = k / NC, s = R::slot(c, i);
-        if (i >= SPC && !mbar_wait(empty + s, R::phase(i - SPC), limit_ns)) {
-            set_status(status, kStatusWaitEmpty);
-            failed |= kStatusWaitEmpty;
-            break;
-        }
-        issue(k, s);
-        issued = k + 1;
+    // Wait for unit i on the warp's barriers `full` (SPC of them).
+    __device__ __forceinline__ static bool wait(uint64_t *full, int i, unsigned long long limit_ns)
+    {
+        return mbar_wait(full + slot(i), phase(i), limit_ns);
     }
-    // drain: the last copy issued into each slot (earlier ones have landed,
-    // since a slot is refilled only after its consumer released it)
-    for (int k = issued - 1; k >= 0 && k >= issued - R::S; --k) {
-        const int c = k % NC, i = k / NC;
-        if (!mbar_wait(full + R::slot(c, i), R::phase(i), limit_ns)) {
-            set_status(status, kStatusWaitDrain);
-            failed |= kStatusWaitDrain;
-            break;
-        }
+
+    // Failure path, after the wait for unit i ran out: wait (bounded again)
+    // for every unit the warp has requested and not consumed, i .. i+SPC-1
+    // below `units`, so that no copy lands after the CTA has exited; record
+    // the failure.  Returns the status bits set.
+    __device__ static unsigned abort(uint64_t *full, int i, int units, unsigned *status,
+                                     unsigned long long limit_ns)
+    {
+        unsigned bits = kStatusWaitFull;
+        for (int u = i; u < i + SPC && u < units; ++u)
+            if (!wait(full, u, limit_ns)) {
+                bits |= kStatusWaitDrain;
+                break;
+            }
+        set_status(status, bits);
+        return bits;
     }
-    return failed;
-}
+};
 
 } // namespace dan

@@ -41,8 +41,6 @@
 #include "dan_internal.h"
 #include "dan_ring.cuh"
 
-#include <mutex>
-#include <unordered_map>
 
 namespace dan {
 
@@ -406,36 +404,37 @@ __device__ __forceinline__ void ln_row(const uint4 (&v)[4][FPT], const RowParams
 
 enum RowKind { kRms = 0, kGated = 1, kLn = 2 };
 
-// Shared memory: the ring of S = NC * SPC row slots (NIN inputs of D bf16
-// each), the norm weight, the staged vectors, then 2 * S mbarriers.
+// Shared memory: NW * SPC row slots (NIN inputs of D bf16 each; warp c
+// owns slots c*SPC .. c*SPC+SPC-1), the norm weight, the staged vectors,
+// then one mbarrier per slot.
 template <int KIND>
 struct RowShape {
     static constexpr int NIN = KIND == kGated ? 2 : 1; // bulk-copied inputs per row
     static constexpr int NV = KIND == kGated ? 3 : 2;  // staged vectors per batch
 };
 
-// CTA c takes the contiguous rows [c*R/G, (c+1)*R/G).  Warp 0 lane 0 is
-// the producer; warps 1..NC are consumers (one row at a time, the whole
-// row in registers: LW logical warps per lane for RMS, 4 for LayerNorm).
+// CTA c takes the contiguous rows [c*R/G, (c+1)*R/G); its warp w takes the
+// CTA's rows w, w + NW, w + 2NW, ... one at a time, the whole row in
+// registers (LW logical warps per lane for RMS, 4 for LayerNorm), and
+// requests each row SPC rows ahead into its own slots (dan_ring.cuh).
 // CTA_STATUS kernels also keep one failure record per CTA in
 // p.cta_status[blockIdx.x], cleared when the CTA starts.
-template <int KIND, int LW, int FPT, int NC, int SPC, bool HAS_W, bool RAGGED, bool STAGED,
+template <int KIND, int LW, int FPT, int NW, int SPC, bool HAS_W, bool RAGGED, bool STAGED,
           bool CTA_STATUS = false>
-__global__ void __launch_bounds__(32 * (NC + 1), 1)
+__global__ void __launch_bounds__(32 * NW, 1)
     row_ring_kernel(const RowParams p, const InvTable2 inv)
 {
     using Shape = RowShape<KIND>;
-    using R = RingSchedule<NC, SPC>;
+    using Pipe = WarpPipe<SPC>;
     constexpr int NIN = Shape::NIN, NV = Shape::NV;
     const int F = p.F;
     const unsigned row_bytes = (unsigned)F * 16u;
 
     extern __shared__ __align__(128) uint4 smem[];
-    uint4 *ring = smem;                              // S * NIN * F
-    uint4 *s_w = ring + (int64_t)R::S * NIN * F;     // F if HAS_W
-    uint4 *s_vec = s_w + (HAS_W ? F : 0);            // Bs * NV * F
+    uint4 *ring = smem;                                 // NW * SPC * NIN * F
+    uint4 *s_w = ring + (int64_t)NW * SPC * NIN * F;    // F if HAS_W
+    uint4 *s_vec = s_w + (HAS_W ? F : 0);               // Bs * NV * F
     uint64_t *full = reinterpret_cast<uint64_t *>(s_vec + (int64_t)p.Bs * NV * F);
-    uint64_t *empty = full + R::S;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t G = gridDim.x;
@@ -443,53 +442,39 @@ __global__ void __launch_bounds__(32 * (NC + 1), 1)
     const int n = (int)((int64_t)(blockIdx.x + 1) * p.rows / G - r0);
 
     if (threadIdx.x == 0) {
-        if (CTA_STATUS) p.cta_status[blockIdx.x] = 0u;
-        for (int s = 0; s < R::S; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
-        }
+        for (int s = 0; s < NW * SPC; ++s) mbar_init(full + s, 1);
         mbar_init_fence();
     }
+    grid_dependency_wait(); // no global access above this line
+    allow_dependents();
+    if (CTA_STATUS && threadIdx.x == 0) p.cta_status[blockIdx.x] = 0u;
     stage_begin<NV, HAS_W>(p, s_w, s_vec);
     __syncthreads(); // barriers initialised
 
-    auto issue = [&](int k, int s) {
-        const int64_t row = r0 + k;
-        uint4 *dst = ring + (int64_t)s * NIN * F;
-        mbar_arrive_expect_tx(full + s, NIN * row_bytes);
-        bulk_load(dst, p.x + row * F, row_bytes, full + s);
-        if (NIN == 2) bulk_load(dst + F, p.h + row * F, row_bytes, full + s);
+    uint4 *slots = ring + (int64_t)warp * SPC * NIN * F;
+    uint64_t *bar = full + warp * SPC;
+    const int units = warp < n ? (n - warp + NW - 1) / NW : 0; // rows of this warp
+    auto request = [&](int i) {                                // lane 0 only
+        const int64_t row = r0 + warp + (int64_t)NW * i;
+        uint4 *dst = slots + (int64_t)Pipe::slot(i) * NIN * F;
+        uint64_t *b = bar + Pipe::slot(i);
+        mbar_arrive_expect_tx(b, NIN * row_bytes);
+        bulk_load(dst, p.x + row * F, row_bytes, b);
+        if (NIN == 2) bulk_load(dst + F, p.h + row * F, row_bytes, b);
     };
-    const bool producer = warp == 0 && lane == 0;
-    // The first ring's worth of rows needs no slot release: issue it before
-    // waiting for the staged vectors.
-    if (producer)
-        for (int k = 0; k < n && k < R::S; ++k) issue(k, R::slot(k % NC, k / NC));
+    // The first SPC rows go out before waiting for the staged vectors.
+    if (lane == 0)
+        for (int i = 0; i < SPC && i < units; ++i) request(i);
     stage_end<NV>(p, s_vec);
 
-    if (warp == 0) {
-        if (producer) {
-            const unsigned failed =
-                ring_produce<NC, SPC>(n, full, empty, p.status, p.limit_ns, [&](int k, int s) {
-                    if (k >= R::S) issue(k, s); // the first S rows were issued above
-                });
-            if (CTA_STATUS && failed) set_status(p.cta_status + blockIdx.x, failed);
-        }
-        return;
-    }
-
-    const int c = warp - 1;
-    for (int i = 0;; ++i) {
-        const int k = c + i * NC;
-        if (k >= n) break;
-        const int s = R::slot(c, i);
-        if (!mbar_wait(full + s, R::phase(i), p.limit_ns)) {
-            set_status(p.status, kStatusWaitFull);
-            if (CTA_STATUS) set_status(p.cta_status + blockIdx.x, kStatusWaitFull);
+    for (int i = 0; i < units; ++i) {
+        if (!Pipe::wait(bar, i, p.limit_ns)) {
+            const unsigned bits = Pipe::abort(bar, i, units, p.status, p.limit_ns);
+            if (CTA_STATUS) set_status(p.cta_status + blockIdx.x, bits);
             return;
         }
-        const uint4 *src = ring + (int64_t)s * NIN * F;
-        const int64_t row = r0 + k;
+        const uint4 *src = slots + (int64_t)Pipe::slot(i) * NIN * F;
+        const int64_t row = r0 + warp + (int64_t)NW * i;
         if (KIND == kLn) {
             uint4 v[4][FPT];
 #pragma unroll
@@ -499,7 +484,8 @@ __global__ void __launch_bounds__(32 * (NC + 1), 1)
                     const int f = ln_frag(j, lane, q);
                     v[j][q] = (!RAGGED || f < F) ? src[f] : make_uint4(0, 0, 0, 0);
                 }
-            ring_release(empty + s, lane);
+            slot_reads_done();
+            if (lane == 0 && i + SPC < units) request(i + SPC);
             ln_row<FPT, RAGGED, STAGED>(v, p, row, inv, s_vec, lane);
         } else {
             uint4 v[LW][8];
@@ -518,7 +504,8 @@ __global__ void __launch_bounds__(32 * (NC + 1), 1)
                                        gated_word(r.z, g.z, hh.z), gated_word(r.w, g.w, hh.w));
                     }
                 }
-            ring_release(empty + s, lane);
+            slot_reads_done();
+            if (lane == 0 && i + SPC < units) request(i + SPC);
             if (KIND == kGated)
 #pragma unroll
                 for (int j = 0; j < LW; ++j)
@@ -537,38 +524,11 @@ namespace {
 constexpr unsigned long long kWaitLimitNs = 1000000000ull; // 1 s per wait
 constexpr int kStageBudget = 96 * 1024; // most shared memory staged vectors may take
 
-std::mutex g_mu;
-std::unordered_map<const void *, int> g_smem_set; // kernel -> max dyn smem configured
-
-int max_smem_optin()
-{
-    static int cache[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int &c = cache[dev & 63];
-    if (c == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-            v <= 0)
-            v = 48 * 1024;
-        c = v;
-    }
-    return c;
-}
-
 // Raise the dynamic shared-memory limit of `fn` the first time it needs more.
 template <typename K>
 cudaError_t allow_smem(K fn, int smem)
 {
-    std::lock_guard<std::mutex> lk(g_mu);
-    const void *key = reinterpret_cast<const void *>(fn);
-    auto it = g_smem_set.find(key);
-    if (smem > 48 * 1024 && (it == g_smem_set.end() || it->second < smem)) {
-        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        g_smem_set[key] = smem;
-    }
-    return cudaSuccess;
+    return allow_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
 }
 
 RowParams make_params(const RowProblem &q)
@@ -605,35 +565,45 @@ InvTable2 inv_table()
     return inv;
 }
 
-// One CTA per SM (the ring and the consumers' registers fill it); each CTA
-// takes a contiguous block of rows.
-template <int KIND, int LW, int FPT, int NC, int SPC, bool RAGGED>
-cudaError_t launch_ring(const RowProblem &q, cudaStream_t s)
+// Shared memory a launch of row_ring_kernel<KIND, ..., NW, SPC> needs, with
+// p.Bs set to the number of batches whose vectors are staged (all of them
+// when they fit in the staging budget, else none).
+template <int KIND, int NW, int SPC>
+int ring_smem(const RowProblem &q, RowParams &p)
 {
     using Shape = RowShape<KIND>;
-    constexpr int S = NC * SPC;
-    RowParams p = make_params(q);
-    const bool has_w = q.weight != nullptr;
     const int64_t row_bytes = q.D * 2;
-    const int64_t fixed = (int64_t)S * Shape::NIN * row_bytes + (has_w ? row_bytes : 0) + 2 * S * 8;
+    const int64_t fixed = (int64_t)NW * SPC * Shape::NIN * row_bytes +
+                          (KIND != kLn && q.weight ? row_bytes : 0) + NW * SPC * 8;
     const int64_t vec_bytes = q.B * Shape::NV * row_bytes;
     const int64_t room = (int64_t)max_smem_optin() - fixed;
     p.Bs = (vec_bytes <= kStageBudget && vec_bytes <= room) ? (int)q.B : 0;
-    const int smem = (int)(fixed + (p.Bs ? vec_bytes : 0));
-    const int64_t grid64 = p.rows < sm_count() ? p.rows : sm_count();
-    const int grid = (int)grid64;
+    return (int)(fixed + (p.Bs ? vec_bytes : 0));
+}
+
+// One CTA per SM (the slots and the warps' registers fill it), at most one
+// per row; each CTA takes a contiguous block of rows.  `cta_status` is the
+// per-CTA failure record array of CTA_STATUS kernels (nullptr otherwise).
+template <int KIND, int LW, int FPT, int NW, int SPC, bool RAGGED, bool CTA_STATUS = false>
+cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr)
+{
+    RowParams p = make_params(q);
+    p.cta_status = cta_status;
+    const bool has_w = KIND != kLn && q.weight != nullptr;
+    const int smem = ring_smem<KIND, NW, SPC>(q, p);
+    const int grid = (int)(p.rows < sm_count() ? p.rows : sm_count());
     const InvTable2 inv = inv_table();
     auto go = [&](auto fn) -> cudaError_t {
         const cudaError_t e = allow_smem(fn, smem);
         if (e != cudaSuccess) return e;
-        fn<<<grid, 32 * (NC + 1), smem, s>>>(p, inv);
-        return cudaGetLastError();
+        return launch_overlapped(fn, grid, 32 * NW, smem, s, p, inv);
     };
-    if (KIND != kLn && has_w)
-        return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NC, SPC, KIND != kLn, RAGGED, true>)
-                    : go(row_ring_kernel<KIND, LW, FPT, NC, SPC, KIND != kLn, RAGGED, false>);
-    return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NC, SPC, false, RAGGED, true>)
-                : go(row_ring_kernel<KIND, LW, FPT, NC, SPC, false, RAGGED, false>);
+    constexpr bool CS = CTA_STATUS;
+    if (has_w)
+        return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, SPC, true, RAGGED, true, CS>)
+                    : go(row_ring_kernel<KIND, LW, FPT, NW, SPC, true, RAGGED, false, CS>);
+    return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, SPC, false, RAGGED, true, CS>)
+                : go(row_ring_kernel<KIND, LW, FPT, NW, SPC, false, RAGGED, false, CS>);
 }
 
 template <bool RAGGED>
@@ -644,10 +614,10 @@ cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
     case 2: return launch_ring<kLn, 4, 2, 8, 1, RAGGED>(q, s);
     case 3: return launch_ring<kLn, 4, 3, 8, 1, RAGGED>(q, s);
     case 4: return launch_ring<kLn, 4, 4, 8, 1, RAGGED>(q, s);
-    case 5: return launch_ring<kLn, 4, 5, 4, 2, RAGGED>(q, s);
-    case 6: return launch_ring<kLn, 4, 6, 4, 2, RAGGED>(q, s);
-    case 7: return launch_ring<kLn, 4, 7, 4, 2, RAGGED>(q, s);
-    default: return launch_ring<kLn, 4, 8, 4, 2, RAGGED>(q, s);
+    case 5: return launch_ring<kLn, 4, 5, 8, 1, RAGGED>(q, s);
+    case 6: return launch_ring<kLn, 4, 6, 8, 1, RAGGED>(q, s);
+    case 7: return launch_ring<kLn, 4, 7, 8, 1, RAGGED>(q, s);
+    default: return launch_ring<kLn, 4, 8, 8, 1, RAGGED>(q, s);
     }
 }
 

@@ -82,8 +82,9 @@ const char *dan_status_string(int status);
  * completion they wait for on mbarriers.  Every such wait is bounded (about
  * one second); a wait that runs out makes the kernel record a bit in the
  * current device's status word and return, leaving its outputs incomplete:
- *   1 = a consumer gave up on a row, 2 = the producer gave up on a slot,
- *   4 = the producer gave up waiting for its own copies.
+ *   1 = a warp gave up waiting for a row (or head group) it had requested,
+ *   4 = after that, it also gave up waiting for its other copies in flight.
+ * (Bit 2 is not used.)
  * dan_get_device_status reads the word of the current device into *status
  * and clears it.  It is synchronous: call it after synchronising the streams
  * the kernels ran on.  Returns DAN_OK, DAN_EINVAL (status NULL) or DAN_ECUDA.
