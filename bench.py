@@ -438,6 +438,11 @@ def run_ours(args, rank, world, dist):
             b, r = kb[name]
             per_kernel[name] = {"us_per_launch": us, "gbs": b / us / 1e3, "rows_per_s": r / us * 1e6,
                                 "bytes_per_launch": b, "rows_per_launch": r}
+    configs = None
+    if not args.no_configs:
+        t0 = time.time()
+        configs = time_configs(dev, stream)
+        clocks.mark(t0, time.time())
     clock_info = clocks.stop()
 
     # e2e through the public API with pinned host buffers: every step copies
@@ -523,6 +528,8 @@ def run_ours(args, rank, world, dist):
                             "the previous kernel drains (programmatic dependent launch)"},
         "hbm_frac": agg["gbs"] / world / peak, "rows_per_s": agg["rows_per_s"],
         "kernels": {n: dict(v, hbm_frac=v["gbs"] / peak) for n, v in per_kernel.items()},
+        "configs": ({n: dict(v, hbm_frac=v["gbs"] / peak) for n, v in configs.items()}
+                    if configs is not None else None),
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": pk["gbs"], "peak": peak,
                      "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback",
@@ -540,6 +547,114 @@ def run_ours(args, rank, world, dist):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(h)
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------- every configuration
+
+# The kernel configurations of the path: the metric's shapes and the
+# pages' other sites (FLUX.1 LayerNorm sites at D = 3072, the CFG batch of
+# two, the ERNIE RMS with weight at the larger hidden sizes).  Each is timed
+# alone; these are per-kernel figures, not part of the step.
+CONFIGS = [
+    ("C1 rms [1,128,2048]", "rms", 1, 128, 2048, False),
+    ("C1' rms [1,4216,4096]", "rms", 1, 4216, 4096, False),
+    ("C2a ln [1,4096,3072]", "ln", 1, 4096, 3072, False),
+    ("C2b ln [1,512,3072]", "ln", 1, 512, 3072, False),
+    ("C2c ln [1,4608,3072]", "ln", 1, 4608, 3072, False),
+    ("C2d ln [1,4093,3072]", "ln", 1, 4093, 3072, False),
+    ("C2' ln [1,4216,4096]", "ln", 1, 4216, 4096, False),
+    ("C3 gated [1,4216,4096]", "gated", 1, 4216, 4096, False),
+    ("C4 ln CFG [2,1140,4096]", "ln", 2, 1140, 4096, False),
+    ("C5 qk 256+4096 tokens x 24 heads x 128", "qk", 1, 0, 0, False),
+    ("N4 rms+weight [1,4216,6144]", "rms", 1, 4216, 6144, True),
+    ("N4 rms+weight [1,4216,8192]", "rms", 1, 4216, 8192, True),
+    ("N4 gated [1,4216,8192]", "gated", 1, 4216, 8192, False),
+]
+
+
+def config_bytes(kind, B, T, D, weight):
+    """Algorithmic bytes and rows of one launch of a configuration."""
+    if kind == "qk":
+        return kernel_bytes()["qk_norm_rope_epilogue"]
+    rows, nvec = B * T, {"rms": 2, "ln": 2, "gated": 3}[kind]
+    io = {"rms": 2, "ln": 2, "gated": 4}[kind]
+    return io * rows * D * 2 + nvec * B * D * 2 + (D * 2 if weight else 0), rows
+
+
+def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
+    """Launch time of every configuration: a graph of launches cycling over
+    enough buffer sets that ~2x L2 of other traffic separates two uses of a
+    buffer (up to max_sets; smaller configurations stay L2-resident and say
+    so).  Inputs are drawn on the device (normal, seeded): the kernels'
+    time does not depend on the values."""
+    import torch
+    from dit_adaln_norm_gb300 import ops
+    from dit_adaln_norm_gb300.synth import split_qkv
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    rnd = lambda *shape, std=1.0: (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
+    out = {}
+    for name, kind, B, T, D, weight in CONFIGS:
+        nbytes, rows = config_bytes(kind, B, T, D, weight)
+        nsets = max(2, min(max_sets, -(-min_bytes // nbytes)))
+        sets = []
+        for _ in range(nsets):
+            if kind == "qk":
+                txt, img = rnd(T_TXT, 3 * HEADS * 128), rnd(T_IMG, 3 * HEADS * 128)
+                w = (1.0 + rnd(4, 128, std=0.05).float()).to(torch.bfloat16)
+                sets.append(dict(txt=txt, img=img, w=w,
+                                 out=tuple(torch.empty((T_TXT + T_IMG, HEADS, 128),
+                                                       dtype=torch.bfloat16, device=dev)
+                                           for _ in range(3))))
+            else:
+                emb = rnd(B, 6 * D, std=0.1)
+                st = dict(x=rnd(B, T, D), emb=emb, y=torch.empty(B, T, D, dtype=torch.bfloat16, device=dev),
+                          w=(1.0 + rnd(D, std=0.05).float()).to(torch.bfloat16) if weight else None)
+                if kind == "gated":
+                    st.update(h=rnd(B, T, D), r_out=torch.empty(B, T, D, dtype=torch.bfloat16, device=dev))
+                sets.append(st)
+        if kind == "qk":
+            from dit_adaln_norm_gb300 import synth
+            rope_t = torch.from_numpy(synth.rope_table(T_TXT)).to(dev)
+            rope_i = torch.from_numpy(synth.rope_table(T_IMG, pos0=T_TXT)).to(dev)
+
+        def launch(st):
+            if kind == "qk":
+                w = st["w"]
+                ops.qk_norm_rope_epilogue(split_qkv(st["txt"], HEADS), split_qkv(st["img"], HEADS),
+                                          w[0], w[1], w[2], w[3], rope_t, rope_i, EPS, EPS, HEADS,
+                                          out=st["out"])
+                return
+            vec = lambda i: st["emb"][:, i * D:(i + 1) * D]
+            if kind == "rms":
+                ops.rms_modulate(st["x"], vec(0), vec(1), EPS, weight=st["w"], out=st["y"])
+            elif kind == "ln":
+                ops.ln_modulate(st["x"], vec(0), vec(1), EPS, out=st["y"])
+            else:
+                ops.gated_rms_modulate(st["x"], st["h"], vec(0), vec(1), vec(2), EPS,
+                                       r_out=st["r_out"], out=st["y"])
+
+        reps = max(32, nsets)
+        torch.cuda.synchronize()  # inputs were drawn on the default stream
+        with torch.cuda.stream(stream):
+            for st in sets:
+                launch(st)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(reps):
+                    launch(sets[i % nsets])
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            el = time_graphs([graph], n_iter, stream)
+        us = el / (n_iter * reps) * 1e6
+        out[name] = {"us_per_launch": us, "gbs": nbytes / us / 1e3, "rows_per_s": rows / us * 1e6,
+                     "bytes_per_launch": nbytes, "rows_per_launch": rows, "buffer_sets": nsets,
+                     "l2_resident": nsets * nbytes < min_bytes}
+        del sets, graph
+        torch.cuda.empty_cache()
+    return out
 
 
 def kernel_sources_digest():
@@ -575,6 +690,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration kernel timings")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

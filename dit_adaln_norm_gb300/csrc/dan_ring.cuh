@@ -90,6 +90,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
     return false;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // 1-D bulk copy global -> shared of `bytes` (multiple of 16, both addresses
 // 16-byte aligned) completing on `bar`.
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, unsigned bytes,

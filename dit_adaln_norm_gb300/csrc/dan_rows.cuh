@@ -141,80 +141,152 @@ __device__ __forceinline__ int rms_frag(int j, int b, int lane)
     return (32 * LW) * b + 32 * j + lane;
 }
 
-// Canonical sum of squares, rstd, normalise, modulate and store for one
-// row whose fragments are in v (for the gated form v already holds r').
-template <int LW, int NV, bool HAS_W, bool STAGED>
-__device__ __forceinline__ void rms_row(const uint4 (&v)[LW][8], const RowParams &p, int64_t row,
-                                        const uint4 *s_w, const uint4 *s_vec, int lane)
+// The eight bf16 elements of a fragment widened to fp32 (exact).  A row's
+// part is widened once, when it is copied out of its slot, and both the
+// statistics and the normalisation read the fp32 values.
+__device__ __forceinline__ void widen8(const uint4 &f, float (&o)[8])
 {
-    constexpr int TPR = 32 * LW, F = 8 * TPR, D = 8 * F;
-    constexpr int P2 = LW <= 1 ? 1 : LW <= 2 ? 2 : 4;
-    constexpr int NP = LW / 2; // packed chain pairs per lane
-    const int64_t bidx = row / p.T;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        o[2 * w] = lo_f(word(f, w));
+        o[2 * w + 1] = hi_f(word(f, w));
+    }
+}
 
-    // Sum of squares: one ordered chain per logical thread (v fastest, then
-    // the fragment index); logical threads j, j+1 of a lane share packed
-    // multiplies.
-    float acc[LW];
-    {
+// Packed operations take one element from each of two logical warps (j, j+1)
+// when a lane holds an even number of them, else two neighbouring elements
+// of one logical warp; the statistics and the normalisation pair them the
+// same way, so each pair stays in one register pair.
+
+// Canonical sum of squares of LWW logical warps of a row held in x: one
+// ordered chain per logical thread (v fastest, then the fragment index),
+// then the butterfly over the 32 lanes (= the adjacent-pair tree).  Every
+// lane ends with each logical warp's sum.
+template <int LWW>
+__device__ __forceinline__ void rms_sums(const float (&x)[LWW][8][8], float (&acc)[LWW])
+{
+    static_assert(LWW == 1 || LWW % 2 == 0, "one or an even number of logical warps");
+    if (LWW == 1) {
+        float a = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const float2 x2 = make_float2(x[0][k][e], x[0][k][e + 1]);
+                const float2 p = mul2(x2, x2); // two products of one chain, added in order
+                a = __fadd_rn(a, p.x);
+                a = __fadd_rn(a, p.y);
+            }
+        acc[0] = a;
+    } else {
+        constexpr int NP = LWW / 2;
         float2 acc2[NP > 0 ? NP : 1];
-        float acc1 = 0.0f;
 #pragma unroll
         for (int q = 0; q < NP; ++q) acc2[q] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < 8; ++e)
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
-                    const float2 x2 = make_float2(elem(v[2 * q][k], e), elem(v[2 * q + 1][k], e));
+                    const float2 x2 = make_float2(x[2 * q][k][e], x[2 * q + 1][k][e]);
                     acc2[q] = addmul2(acc2[q], x2, x2);
                 }
-                if (LW & 1) {
-                    const float xv = elem(v[LW - 1][k], e);
-                    acc1 = __fadd_rn(acc1, __fmul_rn(xv, xv));
-                }
-            }
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             acc[2 * q] = acc2[q].x;
             acc[2 * q + 1] = acc2[q].y;
         }
-        if (LW & 1) acc[LW - 1] = acc1;
     }
-    // Adjacent-pair tree over the 32 lanes of each logical warp, then over
-    // the logical warp sums padded with +0.
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1)
 #pragma unroll
-        for (int j = 0; j < LW; ++j) acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(kFull, acc[j], off));
+        for (int j = 0; j < LWW; ++j) acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(kFull, acc[j], off));
+}
+
+// rstd of a row from its LW logical warp sums: the adjacent-pair tree padded
+// with +0, then rn(1 / rn(sqrt(rn(rn(s / D) + eps)))).
+template <int LW>
+__device__ __forceinline__ float rms_rstd(const float (&sums)[LW], float eps)
+{
+    constexpr int P2 = LW <= 1 ? 1 : LW <= 2 ? 2 : 4;
+    constexpr int D = 2048 * LW;
     float t[P2];
 #pragma unroll
-    for (int k = 0; k < P2; ++k) t[k] = k < LW ? acc[k] : 0.0f;
+    for (int k = 0; k < P2; ++k) t[k] = k < LW ? sums[k] : 0.0f;
 #pragma unroll
     for (int off = 1; off < P2; off <<= 1)
 #pragma unroll
         for (int k = 0; k < P2; k += 2 * off) t[k] = __fadd_rn(t[k], t[k + off]);
-    const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(t[0], (float)D), p.eps)));
+    return defined_rsqrt(__fadd_rn(__fdiv_rn(t[0], (float)D), eps));
+}
 
+// Modulate two rows of normalised fp32 values t[e] (one fragment) and store:
+// y = bf16(bf16(bf16(t) * o) + shift).
+__device__ __forceinline__ void modulate_store(uint4 *dst, const float (&t)[8], const uint4 &o,
+                                               const uint4 &sh)
+{
+    uint4 out;
 #pragma unroll
-    for (int j = 0; j < LW; ++j)
+    for (int w = 0; w < 4; ++w)
+        set_word(out, w, modulate_word(pack_bf16(t[2 * w], t[2 * w + 1]), word(o, w), word(sh, w)));
+    st_stream(dst, out);
+}
+
+// Normalise, modulate and store the logical warps j0 .. j0+LWW-1 of a row
+// (for the gated form x already holds r').
+template <int LW, int LWW, int NV, bool HAS_W, bool STAGED>
+__device__ __forceinline__ void rms_store(const float (&x)[LWW][8][8], int j0, float rstd,
+                                          const RowParams &p, int64_t row, const uint4 *s_w,
+                                          const uint4 *s_vec, int lane)
+{
+    constexpr int F = 8 * 32 * LW;
+    const int64_t bidx = row / p.T;
+    const float2 rstd2 = dup2(rstd);
+    uint4 *y = p.y + row * F;
+    if (LWW == 1) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const int f = rms_frag<LW>(j, k, lane);
-            const uint4 o = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 0);
-            const uint4 sh = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 1);
+            const int f = rms_frag<LW>(j0, k, lane);
             uint4 wv = make_uint4(0, 0, 0, 0);
             if (HAS_W) wv = s_w[f];
-            uint4 out;
+            float t[8];
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                float2 t2 = mul2(wide2(word(v[j][k], w)), rstd2);
-                if (HAS_W) t2 = mul2(t2, wide2(word(wv, w)));
-                set_word(out, w, modulate_word(pack_bf16(t2.x, t2.y), word(o, w), word(sh, w)));
+            for (int e = 0; e < 8; e += 2) {
+                float2 t2 = mul2(make_float2(x[0][k][e], x[0][k][e + 1]), rstd2);
+                if (HAS_W) t2 = mul2(t2, wide2(word(wv, e / 2)));
+                t[e] = t2.x;
+                t[e + 1] = t2.y;
             }
-            st_stream(p.y + row * F + f, out);
+            modulate_store(y + f, t, vec_frag<NV, STAGED>(p, s_vec, bidx, f, 0),
+                           vec_frag<NV, STAGED>(p, s_vec, bidx, f, 1));
         }
+    } else {
+#pragma unroll
+        for (int q = 0; q < LWW / 2; ++q)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int f0 = rms_frag<LW>(j0 + 2 * q, k, lane);
+                const int f1 = rms_frag<LW>(j0 + 2 * q + 1, k, lane);
+                uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                if (HAS_W) {
+                    w0 = s_w[f0];
+                    w1 = s_w[f1];
+                }
+                float t0[8], t1[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float2 t2 = mul2(make_float2(x[2 * q][k][e], x[2 * q + 1][k][e]), rstd2);
+                    if (HAS_W) t2 = mul2(t2, make_float2(elem(w0, e), elem(w1, e)));
+                    t0[e] = t2.x;
+                    t1[e] = t2.y;
+                }
+                modulate_store(y + f0, t0, vec_frag<NV, STAGED>(p, s_vec, bidx, f0, 0),
+                               vec_frag<NV, STAGED>(p, s_vec, bidx, f0, 1));
+                modulate_store(y + f1, t1, vec_frag<NV, STAGED>(p, s_vec, bidx, f1, 0),
+                               vec_frag<NV, STAGED>(p, s_vec, bidx, f1, 1));
+            }
+    }
 }
 
 // ------------------------------------------------------------ LayerNorm
@@ -280,59 +352,71 @@ struct InvTable2 {
 // Fragment of logical thread t = 32j + lane at its k-th visit: t + 128k.
 __device__ __forceinline__ int ln_frag(int j, int lane, int k) { return 32 * j + lane + 128 * k; }
 
-// One LayerNorm row (4 logical warps in one physical warp): statistics in
-// the canonical Welford order, then normalise, modulate and store.
-template <int FPT, bool RAGGED, bool STAGED>
-__device__ __forceinline__ void ln_row(const uint4 (&v)[4][FPT], const RowParams &p, int64_t row,
-                                       const InvTable2 &inv, const uint4 *s_vec, int lane)
+// Welford states of the J logical warps j = r + TW*m (m = 0..J-1) of a row
+// held in x, each folded over its 32 threads in the canonical order; every
+// lane ends with the states.
+template <int FPT, int J, int TW, bool RAGGED>
+__device__ __forceinline__ void ln_states(const float (&x)[J][FPT][8], int r, int F,
+                                          const InvTable2 &inv, int lane, Welford (&W)[J])
 {
-    constexpr int NV = 2;
-    const int F = p.F;
-    const int64_t bidx = row / p.T;
-    float wmean[4], wm2[4]; // per logical warp, folded over its 32 threads
-
     if (!RAGGED) {
         // Every logical thread holds FPT full fragments: counts are equal
-        // everywhere, so each combine has c = 1/2 exactly.
-        float2 mean2[2], m22[2];
+        // everywhere, so each combine has c = 1/2 exactly.  Logical warps
+        // m, m+1 of a lane share packed operations.
+        constexpr int NP = J / 2;
+        float2 mean2[NP > 0 ? NP : 1], m22[NP > 0 ? NP : 1];
+        float mean1 = 0.0f, m21 = 0.0f;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) mean2[q] = m22[q] = make_float2(0.0f, 0.0f);
+        for (int q = 0; q < NP; ++q) mean2[q] = m22[q] = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < FPT; ++k)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float2 r = inv.v[8 * k + e + 1];
+                const float2 rr = inv.v[8 * k + e + 1];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const float2 x2 = make_float2(elem(v[2 * q][k], e), elem(v[2 * q + 1][k], e));
+                for (int q = 0; q < NP; ++q) {
+                    const float2 x2 = make_float2(x[2 * q][k][e], x[2 * q + 1][k][e]);
                     const float2 d = sub2(x2, mean2[q]);
-                    mean2[q] = addmul2(mean2[q], d, r);
+                    mean2[q] = addmul2(mean2[q], d, rr);
                     m22[q] = addmul2(m22[q], d, sub2(x2, mean2[q]));
+                }
+                if (J & 1) {
+                    const float xv = x[J - 1][k][e];
+                    const float d = __fsub_rn(xv, mean1);
+                    mean1 = __fadd_rn(mean1, __fmul_rn(d, rr.x));
+                    m21 = __fadd_rn(m21, __fmul_rn(d, __fsub_rn(xv, mean1)));
                 }
             }
         float nA = (float)(8 * FPT);
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) {
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
+            for (int q = 0; q < NP; ++q) {
                 const float2 mb = make_float2(__shfl_down_sync(kFull, mean2[q].x, off),
                                               __shfl_down_sync(kFull, mean2[q].y, off));
                 const float2 m2b = make_float2(__shfl_down_sync(kFull, m22[q].x, off),
                                                __shfl_down_sync(kFull, m22[q].y, off));
                 combine_eq2(mean2[q], m22[q], mb, m2b, nA);
             }
+            if (J & 1) {
+                const float mb = __shfl_down_sync(kFull, mean1, off);
+                const float m2b = __shfl_down_sync(kFull, m21, off);
+                combine_eq1(mean1, m21, mb, m2b, nA);
+            }
             nA = 2.0f * nA;
         }
+        const float nw = (float)(256 * FPT);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            wmean[2 * q] = __shfl_sync(kFull, mean2[q].x, 0);
-            wmean[2 * q + 1] = __shfl_sync(kFull, mean2[q].y, 0);
-            wm2[2 * q] = __shfl_sync(kFull, m22[q].x, 0);
-            wm2[2 * q + 1] = __shfl_sync(kFull, m22[q].y, 0);
+        for (int q = 0; q < NP; ++q) {
+            W[2 * q] = Welford{nw, __shfl_sync(kFull, mean2[q].x, 0), __shfl_sync(kFull, m22[q].x, 0)};
+            W[2 * q + 1] =
+                Welford{nw, __shfl_sync(kFull, mean2[q].y, 0), __shfl_sync(kFull, m22[q].y, 0)};
         }
+        if (J & 1) W[J - 1] = Welford{nw, __shfl_sync(kFull, mean1, 0), __shfl_sync(kFull, m21, 0)};
     } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int m = 0; m < J; ++m) {
+            const int j = r + TW * m;
             float mean = 0.0f, m2 = 0.0f;
             int nfr = 0;
 #pragma unroll
@@ -341,108 +425,162 @@ __device__ __forceinline__ void ln_row(const uint4 (&v)[4][FPT], const RowParams
                     nfr = k + 1;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float xv = elem(v[j][k], e);
+                        const float xv = x[m][k][e];
                         const float d = __fsub_rn(xv, mean);
                         mean = __fadd_rn(mean, __fmul_rn(d, inv.v[8 * k + e + 1].x));
                         m2 = __fadd_rn(m2, __fmul_rn(d, __fsub_rn(xv, mean)));
                     }
                 }
             }
-            Welford st{(float)(8 * nfr), mean, m2};
-            st = warp_fold(st, lane);
-            wmean[j] = st.mean;
-            wm2[j] = st.m2;
+            W[m] = warp_fold(Welford{(float)(8 * nfr), mean, m2}, lane);
         }
     }
+}
 
-    // The four logical warps: (W0 + W2) + (W1 + W3).
-    float mean, m2;
+// Mean and m2 of a row from its four logical warp states: (W0 + W2) + (W1 + W3).
+template <bool RAGGED>
+__device__ __forceinline__ void ln_final(const Welford (&W)[4], float &mean, float &m2)
+{
     if (!RAGGED) {
-        const float nw = (float)(256 * FPT); // count of one logical warp
-        float2 m01 = make_float2(wmean[0], wmean[1]), q01 = make_float2(wm2[0], wm2[1]);
-        combine_eq2(m01, q01, make_float2(wmean[2], wmean[3]), make_float2(wm2[2], wm2[3]), nw);
+        const float nw = W[0].n; // all four counts are equal
+        float2 m01 = make_float2(W[0].mean, W[1].mean), q01 = make_float2(W[0].m2, W[1].m2);
+        combine_eq2(m01, q01, make_float2(W[2].mean, W[3].mean), make_float2(W[2].m2, W[3].m2), nw);
         mean = m01.x;
         m2 = q01.x;
         combine_eq1(mean, m2, m01.y, q01.y, 2.0f * nw);
     } else {
-        float N[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            int cnt = 0; // 8 per valid fragment of the logical warp's threads
-            for (int t = 32 * j; t < 32 * j + 32; ++t)
-                for (int k = 0; k < FPT; ++k) cnt += (t + 128 * k < F) ? 8 : 0;
-            N[j] = (float)cnt;
-        }
-        const Welford S =
-            combine(combine(Welford{N[0], wmean[0], wm2[0]}, Welford{N[2], wmean[2], wm2[2]}),
-                    combine(Welford{N[1], wmean[1], wm2[1]}, Welford{N[3], wmean[3], wm2[3]}));
+        const Welford S = combine(combine(W[0], W[2]), combine(W[1], W[3]));
         mean = S.mean;
         m2 = S.m2;
     }
-    const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
-    const float2 mean2 = dup2(mean);
-
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int k = 0; k < FPT; ++k) {
-            const int f = ln_frag(j, lane, k);
-            if (RAGGED && f >= F) continue;
-            const uint4 o = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 0);
-            const uint4 sh = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 1);
-            uint4 out;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float2 t2 = mul2(sub2(wide2(word(v[j][k], w)), mean2), rstd2);
-                set_word(out, w, modulate_word(pack_bf16(t2.x, t2.y), word(o, w), word(sh, w)));
-            }
-            st_stream(p.y + row * F + f, out);
-        }
 }
 
-// ------------------------------------------------------- the ring kernel
+// Normalise, modulate and store the logical warps r + TW*m of a row.
+template <int FPT, int J, int TW, bool RAGGED, bool STAGED>
+__device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, float mean, float m2,
+                                         const RowParams &p, int64_t row, const uint4 *s_vec,
+                                         int lane)
+{
+    constexpr int NV = 2;
+    const int F = p.F;
+    const int64_t bidx = row / p.T;
+    const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
+    const float2 mean2 = dup2(mean);
+    uint4 *y = p.y + row * F;
+    if (!RAGGED && J >= 2) { // pairs across logical warps, as in ln_states
+#pragma unroll
+        for (int q = 0; q < J / 2; ++q)
+#pragma unroll
+            for (int k = 0; k < FPT; ++k) {
+                const int f0 = ln_frag(r + TW * 2 * q, lane, k);
+                const int f1 = ln_frag(r + TW * (2 * q + 1), lane, k);
+                float t0[8], t1[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float2 t2 =
+                        mul2(sub2(make_float2(x[2 * q][k][e], x[2 * q + 1][k][e]), mean2), rstd2);
+                    t0[e] = t2.x;
+                    t1[e] = t2.y;
+                }
+                modulate_store(y + f0, t0, vec_frag<NV, STAGED>(p, s_vec, bidx, f0, 0),
+                               vec_frag<NV, STAGED>(p, s_vec, bidx, f0, 1));
+                modulate_store(y + f1, t1, vec_frag<NV, STAGED>(p, s_vec, bidx, f1, 0),
+                               vec_frag<NV, STAGED>(p, s_vec, bidx, f1, 1));
+            }
+    } else { // neighbouring elements of one logical warp
+#pragma unroll
+        for (int m = 0; m < J; ++m)
+#pragma unroll
+            for (int k = 0; k < FPT; ++k) {
+                const int f = ln_frag(r + TW * m, lane, k);
+                if (RAGGED && f >= F) continue;
+                float t[8];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 t2 = mul2(sub2(make_float2(x[m][k][e], x[m][k][e + 1]), mean2), rstd2);
+                    t[e] = t2.x;
+                    t[e + 1] = t2.y;
+                }
+                modulate_store(y + f, t, vec_frag<NV, STAGED>(p, s_vec, bidx, f, 0),
+                               vec_frag<NV, STAGED>(p, s_vec, bidx, f, 1));
+            }
+    }
+}
+
+// ------------------------------------------------------- the row kernel
 
 enum RowKind { kRms = 0, kGated = 1, kLn = 2 };
 
-// Shared memory: NW * SPC row slots (NIN inputs of D bf16 each; warp c
-// owns slots c*SPC .. c*SPC+SPC-1), the norm weight, the staged vectors,
-// then one mbarrier per slot.
 template <int KIND>
 struct RowShape {
     static constexpr int NIN = KIND == kGated ? 2 : 1; // bulk-copied inputs per row
     static constexpr int NV = KIND == kGated ? 3 : 2;  // staged vectors per batch
 };
 
-// CTA c takes the contiguous rows [c*R/G, (c+1)*R/G); its warp w takes the
-// CTA's rows w, w + NW, w + 2NW, ... one at a time, the whole row in
-// registers (LW logical warps per lane for RMS, 4 for LayerNorm), and
-// requests each row SPC rows ahead into its own slots (dan_ring.cuh).
+// Team exchange: per team and row parity, the logical warp results of a
+// row (RMS: LW sums; LayerNorm: four states of n, mean, m2).
+constexpr int kXchFloats = 16;
+
+// Shared memory: NT = NW / TW teams of TW warps; each team owns SPC row
+// slots (NIN inputs of D bf16 each); then the norm weight, the staged
+// vectors, one mbarrier per slot, two team mbarriers per team (slot read,
+// results published), and the team exchange area.
+template <int KIND, int NW, int TW, int SPC>
+struct RowLayout {
+    static constexpr int NT = NW / TW;
+    static int64_t slots_bytes(int F) { return (int64_t)NT * SPC * RowShape<KIND>::NIN * F * 16; }
+    static constexpr int tail_bytes = NT * SPC * 8 + 2 * NT * 8 + NT * 2 * kXchFloats * 4;
+};
+
+// CTA c takes the contiguous rows [c*R/G, (c+1)*R/G).  Its warps form
+// NT = NW / TW teams; team t takes the CTA's rows t, t + NT, t + 2NT, ...
+// one at a time and requests each row SPC rows ahead into its own slots
+// (dan_ring.cuh).  A row's logical warps (LW for RMS, 4 for LayerNorm) are
+// shared among the team's warps, each holding its part in registers.  The
+// leader refills a slot once every warp of the team has read it (team
+// mbarrier `read`); the warps exchange their logical warp sums or states
+// through shared memory (team mbarrier `done`), and each combines all of
+// them in the canonical order, so the result does not depend on TW.  Every
+// wait is bounded.
 // CTA_STATUS kernels also keep one failure record per CTA in
 // p.cta_status[blockIdx.x], cleared when the CTA starts.
-template <int KIND, int LW, int FPT, int NW, int SPC, bool HAS_W, bool RAGGED, bool STAGED,
-          bool CTA_STATUS = false>
+template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool HAS_W, bool RAGGED,
+          bool STAGED, bool CTA_STATUS = false>
 __global__ void __launch_bounds__(32 * NW, 1)
     row_ring_kernel(const RowParams p, const InvTable2 inv)
 {
     using Shape = RowShape<KIND>;
     using Pipe = WarpPipe<SPC>;
-    constexpr int NIN = Shape::NIN, NV = Shape::NV;
+    using Lay = RowLayout<KIND, NW, TW, SPC>;
+    constexpr int NIN = Shape::NIN, NV = Shape::NV, NT = Lay::NT;
+    constexpr int LWW = KIND == kLn ? 1 : LW / TW; // RMS logical warps per warp
+    constexpr int J = KIND == kLn ? 4 / TW : 1;     // LayerNorm logical warps per warp
+    static_assert(NW % TW == 0, "teams of TW warps");
+    static_assert(KIND == kLn ? (4 % TW == 0) : (LW % TW == 0), "TW divides the logical warps");
     const int F = p.F;
     const unsigned row_bytes = (unsigned)F * 16u;
 
     extern __shared__ __align__(128) uint4 smem[];
-    uint4 *ring = smem;                                 // NW * SPC * NIN * F
-    uint4 *s_w = ring + (int64_t)NW * SPC * NIN * F;    // F if HAS_W
-    uint4 *s_vec = s_w + (HAS_W ? F : 0);               // Bs * NV * F
+    uint4 *ring = smem;                                // NT * SPC * NIN * F
+    uint4 *s_w = ring + (int64_t)NT * SPC * NIN * F;   // F if HAS_W
+    uint4 *s_vec = s_w + (HAS_W ? F : 0);              // Bs * NV * F
     uint64_t *full = reinterpret_cast<uint64_t *>(s_vec + (int64_t)p.Bs * NV * F);
+    uint64_t *read_bar = full + NT * SPC; // per team: every warp has read the slot
+    uint64_t *done_bar = read_bar + NT;    // per team: every warp has published its results
+    float *xch_all = reinterpret_cast<float *>(done_bar + NT);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int team = warp / TW, r = warp % TW;
     const int64_t G = gridDim.x;
     const int64_t r0 = (int64_t)blockIdx.x * p.rows / G;
     const int n = (int)((int64_t)(blockIdx.x + 1) * p.rows / G - r0);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NW * SPC; ++s) mbar_init(full + s, 1);
+        for (int s = 0; s < NT * SPC; ++s) mbar_init(full + s, 1);
+        for (int t = 0; t < NT; ++t) {
+            mbar_init(read_bar + t, TW);
+            mbar_init(done_bar + t, TW);
+        }
         mbar_init_fence();
     }
     grid_dependency_wait(); // no global access above this line
@@ -451,68 +589,139 @@ __global__ void __launch_bounds__(32 * NW, 1)
     stage_begin<NV, HAS_W>(p, s_w, s_vec);
     __syncthreads(); // barriers initialised
 
-    uint4 *slots = ring + (int64_t)warp * SPC * NIN * F;
-    uint64_t *bar = full + warp * SPC;
-    const int units = warp < n ? (n - warp + NW - 1) / NW : 0; // rows of this warp
-    auto request = [&](int i) {                                // lane 0 only
-        const int64_t row = r0 + warp + (int64_t)NW * i;
+    uint4 *slots = ring + (int64_t)team * SPC * NIN * F;
+    uint64_t *bar = full + team * SPC;
+    const int units = team < n ? (n - team + NT - 1) / NT : 0; // rows of this team
+    const bool leader = r == 0 && lane == 0;
+    auto request = [&](int i) { // the team leader only
+        const int64_t row = r0 + team + (int64_t)NT * i;
         uint4 *dst = slots + (int64_t)Pipe::slot(i) * NIN * F;
         uint64_t *b = bar + Pipe::slot(i);
         mbar_arrive_expect_tx(b, NIN * row_bytes);
         bulk_load(dst, p.x + row * F, row_bytes, b);
         if (NIN == 2) bulk_load(dst + F, p.h + row * F, row_bytes, b);
     };
+    auto fail = [&](int i) {
+        const unsigned bits = Pipe::abort(bar, i, units, p.status, p.limit_ns);
+        if (CTA_STATUS) set_status(p.cta_status + blockIdx.x, bits);
+    };
     // The first SPC rows go out before waiting for the staged vectors.
-    if (lane == 0)
+    if (leader)
         for (int i = 0; i < SPC && i < units; ++i) request(i);
     stage_end<NV>(p, s_vec);
 
     for (int i = 0; i < units; ++i) {
         if (!Pipe::wait(bar, i, p.limit_ns)) {
-            const unsigned bits = Pipe::abort(bar, i, units, p.status, p.limit_ns);
-            if (CTA_STATUS) set_status(p.cta_status + blockIdx.x, bits);
+            fail(i);
             return;
         }
         const uint4 *src = slots + (int64_t)Pipe::slot(i) * NIN * F;
-        const int64_t row = r0 + warp + (int64_t)NW * i;
+        const int64_t row = r0 + team + (int64_t)NT * i;
+        float *xch = xch_all + (team * 2 + (i & 1)) * kXchFloats;
+        // After this warp has read the slot (slot_reads_done): the leader
+        // refills it once every warp of the team has read it.  A warp
+        // arrives on `read` for row i+1 only after `done` of row i, which
+        // needs the leader's arrivals of row i, so the phases never mix.
+        auto refill = [&]() -> bool {
+            if (TW > 1) {
+                if (lane == 0) mbar_arrive(read_bar + team);
+                if (r == 0 && !mbar_wait(read_bar + team, (unsigned)i & 1u, p.limit_ns))
+                    return false;
+            }
+            if (leader && i + SPC < units) request(i + SPC);
+            return true;
+        };
+        // Teams of several warps: publish this warp's results (written to
+        // xch by lane 0) and wait for the other warps'.
+        auto publish = [&]() -> bool {
+            if (TW == 1) return true;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(done_bar + team);
+            return mbar_wait(done_bar + team, (unsigned)i & 1u, p.limit_ns);
+        };
         if (KIND == kLn) {
-            uint4 v[4][FPT];
+            float x[J][FPT][8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int m = 0; m < J; ++m)
 #pragma unroll
                 for (int q = 0; q < FPT; ++q) {
-                    const int f = ln_frag(j, lane, q);
-                    v[j][q] = (!RAGGED || f < F) ? src[f] : make_uint4(0, 0, 0, 0);
+                    const int f = ln_frag(r + TW * m, lane, q);
+                    widen8((!RAGGED || f < F) ? src[f] : make_uint4(0, 0, 0, 0), x[m][q]);
                 }
             slot_reads_done();
-            if (lane == 0 && i + SPC < units) request(i + SPC);
-            ln_row<FPT, RAGGED, STAGED>(v, p, row, inv, s_vec, lane);
-        } else {
-            uint4 v[LW][8];
-            const int64_t bidx = row / p.T;
+            if (!refill()) {
+                fail(i);
+                return;
+            }
+            Welford W[J];
+            ln_states<FPT, J, TW, RAGGED>(x, r, F, inv, lane, W);
+            Welford all[4];
+            if (TW == 1) {
 #pragma unroll
-            for (int j = 0; j < LW; ++j)
+                for (int m = 0; m < 4; ++m) all[m] = W[m % J];
+            } else {
+                if (lane == 0)
+#pragma unroll
+                    for (int m = 0; m < J; ++m) {
+                        float *o = xch + 3 * (r + TW * m);
+                        o[0] = W[m].n;
+                        o[1] = W[m].mean;
+                        o[2] = W[m].m2;
+                    }
+            }
+            if (!publish()) {
+                fail(i);
+                return;
+            }
+            if (TW > 1)
+#pragma unroll
+                for (int m = 0; m < 4; ++m) all[m] = Welford{xch[3 * m], xch[3 * m + 1], xch[3 * m + 2]};
+            float mean, m2;
+            ln_final<RAGGED>(all, mean, m2);
+            ln_store<FPT, J, TW, RAGGED, STAGED>(x, r, mean, m2, p, row, s_vec, lane);
+        } else {
+            float x[LWW][8][8];
+            const int64_t bidx = row / p.T;
+            const int j0 = r * LWW;
+#pragma unroll
+            for (int j = 0; j < LWW; ++j)
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const int f = rms_frag<LW>(j, q, lane);
-                    v[j][q] = src[f];
-                    if (KIND == kGated) { // r' = bf16(r + bf16(gate * h))
+                    const int f = rms_frag<LW>(j0 + j, q, lane);
+                    uint4 v = src[f];
+                    if (KIND == kGated) { // r' = bf16(r + bf16(gate * h)), stored at once
                         const uint4 g = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 2);
                         const uint4 hh = src[F + f];
-                        uint4 &r = v[j][q];
-                        r = make_uint4(gated_word(r.x, g.x, hh.x), gated_word(r.y, g.y, hh.y),
-                                       gated_word(r.z, g.z, hh.z), gated_word(r.w, g.w, hh.w));
+                        v = make_uint4(gated_word(v.x, g.x, hh.x), gated_word(v.y, g.y, hh.y),
+                                       gated_word(v.z, g.z, hh.z), gated_word(v.w, g.w, hh.w));
+                        st_stream(p.r_out + row * F + f, v);
                     }
+                    widen8(v, x[j][q]);
                 }
             slot_reads_done();
-            if (lane == 0 && i + SPC < units) request(i + SPC);
-            if (KIND == kGated)
+            if (!refill()) {
+                fail(i);
+                return;
+            }
+            float acc[LWW];
+            rms_sums<LWW>(x, acc);
+            float sums[LW];
+            if (TW == 1) {
 #pragma unroll
-                for (int j = 0; j < LW; ++j)
+                for (int j = 0; j < LW; ++j) sums[j] = acc[j % LWW];
+            } else if (lane == 0) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        st_stream(p.r_out + row * F + rms_frag<LW>(j, q, lane), v[j][q]);
-            rms_row<LW, NV, HAS_W, STAGED>(v, p, row, s_w, s_vec, lane);
+                for (int j = 0; j < LWW; ++j) xch[j0 + j] = acc[j];
+            }
+            if (!publish()) {
+                fail(i);
+                return;
+            }
+            if (TW > 1)
+#pragma unroll
+                for (int j = 0; j < LW; ++j) sums[j] = xch[j];
+            rms_store<LW, LWW, NV, HAS_W, STAGED>(x, j0, rms_rstd<LW>(sums, p.eps), p, row, s_w,
+                                                  s_vec, lane);
         }
     }
 }
@@ -565,16 +774,17 @@ InvTable2 inv_table()
     return inv;
 }
 
-// Shared memory a launch of row_ring_kernel<KIND, ..., NW, SPC> needs, with
-// p.Bs set to the number of batches whose vectors are staged (all of them
-// when they fit in the staging budget, else none).
-template <int KIND, int NW, int SPC>
+// Shared memory a launch of row_ring_kernel<KIND, ..., NW, TW, SPC> needs,
+// with p.Bs set to the number of batches whose vectors are staged (all of
+// them when they fit in the staging budget, else none).
+template <int KIND, int NW, int TW, int SPC>
 int ring_smem(const RowProblem &q, RowParams &p)
 {
     using Shape = RowShape<KIND>;
+    using Lay = RowLayout<KIND, NW, TW, SPC>;
     const int64_t row_bytes = q.D * 2;
-    const int64_t fixed = (int64_t)NW * SPC * Shape::NIN * row_bytes +
-                          (KIND != kLn && q.weight ? row_bytes : 0) + NW * SPC * 8;
+    const int64_t fixed = Lay::slots_bytes((int)(q.D / 8)) +
+                          (KIND != kLn && q.weight ? row_bytes : 0) + Lay::tail_bytes;
     const int64_t vec_bytes = q.B * Shape::NV * row_bytes;
     const int64_t room = (int64_t)max_smem_optin() - fixed;
     p.Bs = (vec_bytes <= kStageBudget && vec_bytes <= room) ? (int)q.B : 0;
@@ -584,13 +794,13 @@ int ring_smem(const RowProblem &q, RowParams &p)
 // One CTA per SM (the slots and the warps' registers fill it), at most one
 // per row; each CTA takes a contiguous block of rows.  `cta_status` is the
 // per-CTA failure record array of CTA_STATUS kernels (nullptr otherwise).
-template <int KIND, int LW, int FPT, int NW, int SPC, bool RAGGED, bool CTA_STATUS = false>
+template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false>
 cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr)
 {
     RowParams p = make_params(q);
     p.cta_status = cta_status;
     const bool has_w = KIND != kLn && q.weight != nullptr;
-    const int smem = ring_smem<KIND, NW, SPC>(q, p);
+    const int smem = ring_smem<KIND, NW, TW, SPC>(q, p);
     const int grid = (int)(p.rows < sm_count() ? p.rows : sm_count());
     const InvTable2 inv = inv_table();
     auto go = [&](auto fn) -> cudaError_t {
@@ -600,24 +810,24 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
     };
     constexpr bool CS = CTA_STATUS;
     if (has_w)
-        return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, SPC, true, RAGGED, true, CS>)
-                    : go(row_ring_kernel<KIND, LW, FPT, NW, SPC, true, RAGGED, false, CS>);
-    return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, SPC, false, RAGGED, true, CS>)
-                : go(row_ring_kernel<KIND, LW, FPT, NW, SPC, false, RAGGED, false, CS>);
+        return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, true, CS>)
+                    : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, false, CS>);
+    return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, true, CS>)
+                : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, false, CS>);
 }
 
 template <bool RAGGED>
 cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
 {
     switch ((q.D + 1023) / 1024) {
-    case 1: return launch_ring<kLn, 4, 1, 8, 1, RAGGED>(q, s);
-    case 2: return launch_ring<kLn, 4, 2, 8, 1, RAGGED>(q, s);
-    case 3: return launch_ring<kLn, 4, 3, 8, 1, RAGGED>(q, s);
-    case 4: return launch_ring<kLn, 4, 4, 8, 1, RAGGED>(q, s);
-    case 5: return launch_ring<kLn, 4, 5, 8, 1, RAGGED>(q, s);
-    case 6: return launch_ring<kLn, 4, 6, 8, 1, RAGGED>(q, s);
-    case 7: return launch_ring<kLn, 4, 7, 8, 1, RAGGED>(q, s);
-    default: return launch_ring<kLn, 4, 8, 8, 1, RAGGED>(q, s);
+    case 1: return launch_ring<kLn, 4, 1, 8, 1, 1, RAGGED>(q, s);
+    case 2: return launch_ring<kLn, 4, 2, 8, 1, 1, RAGGED>(q, s);
+    case 3: return launch_ring<kLn, 4, 3, 8, 1, 1, RAGGED>(q, s);
+    case 4: return launch_ring<kLn, 4, 4, 8, 1, 1, RAGGED>(q, s);
+    case 5: return launch_ring<kLn, 4, 5, 8, 2, 2, RAGGED>(q, s);
+    case 6: return launch_ring<kLn, 4, 6, 8, 2, 2, RAGGED>(q, s);
+    case 7: return launch_ring<kLn, 4, 7, 8, 2, 2, RAGGED>(q, s);
+    default: return launch_ring<kLn, 4, 8, 8, 2, 2, RAGGED>(q, s);
     }
 }
 

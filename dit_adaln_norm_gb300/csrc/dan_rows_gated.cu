@@ -4,15 +4,16 @@
 
 namespace dan {
 
-// Pipeline shapes (warps NW, slots per warp SPC), chosen by measurement at
-// D = 4096 and by the shared memory left for larger rows; a slot holds r and h.
+// Pipeline shapes (warps NW, warps per row TW, slots per team SPC), chosen
+// by measurement at D = 4096 and 8192 and by the shared memory left for
+// larger rows; a slot holds r and h.
 cudaError_t launch_gated_rms_modulate(const RowProblem &q, cudaStream_t s)
 {
     switch (q.D) {
-    case 2048: return launch_ring<kGated, 1, 8, 8, 2, false>(q, s);
-    case 4096: return launch_ring<kGated, 2, 8, 8, 1, false>(q, s);
-    case 6144: return launch_ring<kGated, 3, 8, 6, 1, false>(q, s);
-    default: return launch_ring<kGated, 4, 8, 5, 1, false>(q, s); // 8192
+    case 2048: return launch_ring<kGated, 1, 8, 8, 1, 2, false>(q, s);
+    case 4096: return launch_ring<kGated, 2, 8, 8, 1, 1, false>(q, s);
+    case 6144: return launch_ring<kGated, 3, 8, 6, 3, 1, false>(q, s);
+    default: return launch_ring<kGated, 4, 8, 6, 2, 1, false>(q, s); // 8192: 2 warps per row
     }
 }
 

@@ -3,16 +3,17 @@
 
 namespace dan {
 
-// Pipeline shapes (warps NW, slots per warp SPC), chosen by measurement:
-// eight warps did better than fewer with more slots each, or more warps
-// (which also cap the registers a row needs).
+// Pipeline shapes (warps NW, warps per row TW, slots per team SPC), chosen
+// by measurement: eight single-warp teams did better than fewer teams with
+// more slots each, or more warps (which cap the registers a row needs);
+// rows of 8192 are shared by four warps, which keeps them in registers.
 cudaError_t launch_rms_modulate(const RowProblem &q, cudaStream_t s)
 {
     switch (q.D) {
-    case 2048: return launch_ring<kRms, 1, 8, 8, 2, false>(q, s);
-    case 4096: return launch_ring<kRms, 2, 8, 8, 2, false>(q, s);
-    case 6144: return launch_ring<kRms, 3, 8, 8, 1, false>(q, s);
-    default: return launch_ring<kRms, 4, 8, 8, 1, false>(q, s); // 8192
+    case 2048: return launch_ring<kRms, 1, 8, 8, 1, 2, false>(q, s);
+    case 4096: return launch_ring<kRms, 2, 8, 8, 1, 2, false>(q, s);
+    case 6144: return launch_ring<kRms, 3, 8, 12, 3, 1, false>(q, s);
+    default: return launch_ring<kRms, 4, 8, 16, 4, 1, false>(q, s); // 8192: 4 warps per row
     }
 }
 

@@ -64,6 +64,11 @@ def test_rms_metric_shape():
     run_rms(1, 4216, 4096, synth.SEED_X)
 
 
+def test_rms_wide_rows_shared_by_warps():
+    # rows of 8192 are split over a team of warps: several rows per team
+    run_rms(1, 2000, 8192, 11, weight=True)
+
+
 # ------------------------------------------------------------- gated RMS
 
 def run_gated(B, T, D, seed, weight=False, inplace=False, chunks=6):
@@ -100,6 +105,10 @@ def test_gated_in_place_residual():
 
 def test_gated_many_batches_unstaged_vectors():
     run_gated(5, 6, 4096, 301)
+
+
+def test_gated_wide_rows_shared_by_warps():
+    run_gated(1, 1500, 8192, 12)
 
 
 def test_gated_config():
