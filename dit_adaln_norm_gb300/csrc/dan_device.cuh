@@ -123,15 +123,24 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b)
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a)), "l"(pk2(b)));
     return upk2(r);
 }
-// acc + rn(a * b) per lane, the sum rounded separately.  The product is a
-// packed multiply, the sums are two scalar __fadd_rn: ptxas (CUDA 13.0) was
-// measured to contract a packed mul.rn.f32x2 feeding a packed add.rn.f32x2
-// into one fused multiply-add inside unrolled chains, despite the explicit
-// .rn and --fmad=false, while this split form keeps both roundings.
+// acc + rn(a * b) per lane, the sum rounded separately, for accumulators
+// that are never -0.  ptxas (CUDA 13.0) was measured to contract a packed
+// mul.rn.f32x2 feeding a packed add.rn.f32x2 into one fused multiply-add
+// inside unrolled chains, despite the explicit .rn and --fmad=false (and a
+// fused multiply-add with a -0 addend, the exact identity of a multiply,
+// the same way).  So the product is formed as fma(a, b, +0): that equals
+// rn(a * b) except that a -0 product becomes +0, and acc + (+0) equals
+// acc + (-0) unless acc is -0.  The accumulators this serves (sums of
+// squares, Welford means and m2, and their combines) start at +0 and can
+// never become -0, because a round-to-nearest sum is -0 only when both
+// addends are -0.  Two instructions instead of a multiply and two adds.
 __device__ __forceinline__ float2 addmul2(float2 acc, float2 a, float2 b)
 {
-    const float2 p = mul2(a, b);
-    return make_float2(__fadd_rn(acc.x, p.x), __fadd_rn(acc.y, p.y));
+    const uint64_t pos_zero = 0; // (+0, +0)
+    uint64_t t, r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(pk2(a)), "l"(pk2(b)), "l"(pos_zero));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(acc)), "l"(t));
+    return upk2(r);
 }
 __device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
 // Both elements of a bf16 word as a float2 (low column first).

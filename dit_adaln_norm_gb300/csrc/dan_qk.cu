@@ -62,11 +62,18 @@ struct QkUnit {
 // then Q, K, V, each split in head groups.
 __device__ __forceinline__ void qk_unit(QkUnit &U, const QkParams &p, int64_t t0, int k)
 {
-    const int per_tok = 3 * p.groups;
-    U.tok = t0 + k / per_tok;
-    const int rem = k % per_tok;
-    U.kind = rem / p.groups;
-    U.h0 = (rem % p.groups) * kGroup;
+    if (p.groups == 1) { // up to kGroup heads: one unit per (token, kind); k / 3 by a constant
+        const unsigned uk = (unsigned)k;
+        U.tok = t0 + uk / 3u;
+        U.kind = (int)(uk % 3u);
+        U.h0 = 0;
+    } else {
+        const int per_tok = 3 * p.groups;
+        U.tok = t0 + k / per_tok;
+        const int rem = k % per_tok;
+        U.kind = rem / p.groups;
+        U.h0 = (rem % p.groups) * kGroup;
+    }
     U.s = U.tok < p.T0 ? 0 : 1;
 }
 
@@ -126,19 +133,32 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
         return;
     }
 
-    // Partial sum of squares of each of the lane's heads over its 8 columns
-    // (one ordered chain per head; heads k, k+1 share packed multiplies).
+    // The lane's columns widened to fp32 once; packed operations take the
+    // two columns of one rotation pair (2i, 2i+1) throughout.
+    float x[kHeadsPerLane][8];
+#pragma unroll
+    for (int k = 0; k < kHeadsPerLane; ++k)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            x[k][2 * m] = lo_f(word(U.x[k], m));
+            x[k][2 * m + 1] = hi_f(word(U.x[k], m));
+        }
+
+    // Partial sum of squares of each of the lane's heads over its 8 columns:
+    // one ordered chain per head (two products per packed multiply, added
+    // in column order).
     float ps[16];
 #pragma unroll
-    for (int k = 0; k < kHeadsPerLane; k += 2) {
-        float2 acc = make_float2(0.0f, 0.0f);
+    for (int k = 0; k < kHeadsPerLane; ++k) {
+        float acc = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float2 x2 = make_float2(elem(U.x[k], e), elem(U.x[k + 1], e));
-            acc = addmul2(acc, x2, x2);
+        for (int e = 0; e < 8; e += 2) {
+            const float2 x2 = make_float2(x[k][e], x[k][e + 1]);
+            const float2 sq = mul2(x2, x2);
+            acc = __fadd_rn(acc, sq.x);
+            acc = __fadd_rn(acc, sq.y);
         }
-        ps[k] = acc.x;
-        ps[k + 1] = acc.y;
+        ps[k] = acc;
     }
 #pragma unroll
     for (int k = kHeadsPerLane; k < 16; ++k) ps[k] = 0.0f;
@@ -161,11 +181,17 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
     }
     const float my_rstd = defined_rsqrt(__fadd_rn(__fdiv_rn(ps[0], 128.0f), p.eps[U.s]));
 
+    // cos and sin of the lane's four pairs, each duplicated for a packed
+    // multiply of both members (a, b) of a pair.
     const float cs[4] = {U.c4.x, U.c4.y, U.c4.z, U.c4.w};
     const float sn[4] = {U.s4.x, U.s4.y, U.s4.z, U.s4.w};
-    float2 w2[4];
+    float2 cc[4], ss[4], w2[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) w2[m] = wide2(word(U.w, m));
+    for (int m = 0; m < 4; ++m) {
+        cc[m] = dup2(cs[m]);
+        ss[m] = dup2(sn[m]);
+        w2[m] = wide2(word(U.w, m));
+    }
     const int lane_base = half << 4;
 #pragma unroll
     for (int k = 0; k < kHeadsPerLane; ++k) {
@@ -176,12 +202,11 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
         uint4 out;
 #pragma unroll
         for (int m = 0; m < 4; ++m) { // pair i = 4fl + m: columns 2i, 2i+1
-            const float2 t2 = mul2(mul2(wide2(word(U.x[k], m)), r2), w2[m]);
-            const uint32_t n = pack_bf16(t2.x, t2.y);
-            const float a = lo_f(n), b = hi_f(n);
-            set_word(out, m,
-                     pack_bf16(__fsub_rn(__fmul_rn(a, cs[m]), __fmul_rn(b, sn[m])),
-                               __fadd_rn(__fmul_rn(a, sn[m]), __fmul_rn(b, cs[m]))));
+            const float2 t2 = mul2(mul2(make_float2(x[k][2 * m], x[k][2 * m + 1]), r2), w2[m]);
+            const float2 ab = wide2(pack_bf16(t2.x, t2.y)); // (a, b) rounded to bf16
+            const float2 pc = mul2(ab, cc[m]);              // (rn(a c), rn(b c))
+            const float2 ps2 = mul2(ab, ss[m]);             // (rn(a s), rn(b s))
+            set_word(out, m, pack_bf16(__fsub_rn(pc.x, ps2.y), __fadd_rn(ps2.x, pc.y)));
         }
         if (h < p.H) st_stream(dst + h * 16 + fl, out);
     }

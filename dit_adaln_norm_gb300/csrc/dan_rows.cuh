@@ -237,11 +237,10 @@ __device__ __forceinline__ void modulate_store(uint4 *dst, const float (&t)[8], 
 // (for the gated form x already holds r').
 template <int LW, int LWW, int NV, bool HAS_W, bool STAGED>
 __device__ __forceinline__ void rms_store(const float (&x)[LWW][8][8], int j0, float rstd,
-                                          const RowParams &p, int64_t row, const uint4 *s_w,
-                                          const uint4 *s_vec, int lane)
+                                          const RowParams &p, int64_t row, int64_t bidx,
+                                          const uint4 *s_w, const uint4 *s_vec, int lane)
 {
     constexpr int F = 8 * 32 * LW;
-    const int64_t bidx = row / p.T;
     const float2 rstd2 = dup2(rstd);
     uint4 *y = p.y + row * F;
     if (LWW == 1) {
@@ -458,12 +457,11 @@ __device__ __forceinline__ void ln_final(const Welford (&W)[4], float &mean, flo
 // Normalise, modulate and store the logical warps r + TW*m of a row.
 template <int FPT, int J, int TW, bool RAGGED, bool STAGED>
 __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, float mean, float m2,
-                                         const RowParams &p, int64_t row, const uint4 *s_vec,
-                                         int lane)
+                                         const RowParams &p, int64_t row, int64_t bidx,
+                                         const uint4 *s_vec, int lane)
 {
     constexpr int NV = 2;
     const int F = p.F;
-    const int64_t bidx = row / p.T;
     const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
     const float2 mean2 = dup2(mean);
     uint4 *y = p.y + row * F;
@@ -610,7 +608,20 @@ __global__ void __launch_bounds__(32 * NW, 1)
         for (int i = 0; i < SPC && i < units; ++i) request(i);
     stage_end<NV>(p, s_vec);
 
+    // Batch of the team's current row, kept incrementally (rows step by NT).
+    int64_t bidx = 0, t_in = 0;
+    if (units > 0) {
+        bidx = (r0 + team) / p.T;
+        t_in = (r0 + team) - bidx * p.T;
+    }
     for (int i = 0; i < units; ++i) {
+        if (i > 0) {
+            t_in += NT;
+            while (t_in >= p.T) {
+                t_in -= p.T;
+                ++bidx;
+            }
+        }
         if (!Pipe::wait(bar, i, p.limit_ns)) {
             fail(i);
             return;
@@ -678,10 +689,9 @@ __global__ void __launch_bounds__(32 * NW, 1)
                 for (int m = 0; m < 4; ++m) all[m] = Welford{xch[3 * m], xch[3 * m + 1], xch[3 * m + 2]};
             float mean, m2;
             ln_final<RAGGED>(all, mean, m2);
-            ln_store<FPT, J, TW, RAGGED, STAGED>(x, r, mean, m2, p, row, s_vec, lane);
+            ln_store<FPT, J, TW, RAGGED, STAGED>(x, r, mean, m2, p, row, bidx, s_vec, lane);
         } else {
             float x[LWW][8][8];
-            const int64_t bidx = row / p.T;
             const int j0 = r * LWW;
 #pragma unroll
             for (int j = 0; j < LWW; ++j)
@@ -720,8 +730,8 @@ __global__ void __launch_bounds__(32 * NW, 1)
             if (TW > 1)
 #pragma unroll
                 for (int j = 0; j < LW; ++j) sums[j] = xch[j];
-            rms_store<LW, LWW, NV, HAS_W, STAGED>(x, j0, rms_rstd<LW>(sums, p.eps), p, row, s_w,
-                                                  s_vec, lane);
+            rms_store<LW, LWW, NV, HAS_W, STAGED>(x, j0, rms_rstd<LW>(sums, p.eps), p, row, bidx,
+                                                  s_w, s_vec, lane);
         }
     }
 }
@@ -822,7 +832,7 @@ cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
     switch ((q.D + 1023) / 1024) {
     case 1: return launch_ring<kLn, 4, 1, 8, 1, 1, RAGGED>(q, s);
     case 2: return launch_ring<kLn, 4, 2, 8, 1, 1, RAGGED>(q, s);
-    case 3: return launch_ring<kLn, 4, 3, 8, 1, 1, RAGGED>(q, s);
+    case 3: return launch_ring<kLn, 4, 3, 12, 1, 1, RAGGED>(q, s);
     case 4: return launch_ring<kLn, 4, 4, 8, 1, 1, RAGGED>(q, s);
     case 5: return launch_ring<kLn, 4, 5, 8, 2, 2, RAGGED>(q, s);
     case 6: return launch_ring<kLn, 4, 6, 8, 2, 2, RAGGED>(q, s);
