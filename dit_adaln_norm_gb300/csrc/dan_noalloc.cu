@@ -54,7 +54,10 @@ extern "C" int dan_rms_modulate_noalloc(const dan_bf16 *x, const dan_bf16 *weigh
     switch (D) {
     // the shapes of dan_rms_modulate, with a failure record per CTA
     case 2048: e = dan::launch_ring<dan::kRms, 1, 8, 8, 1, 2, false, true>(q, s, scratch); break;
-    case 4096: e = dan::launch_ring<dan::kRms, 2, 8, 8, 1, 2, false, true>(q, s, scratch); break;
+    case 4096:
+        e = dan::many_rows(q) ? dan::launch_ring<dan::kRms, 2, 8, 12, 1, 2, false, true>(q, s, scratch)
+                              : dan::launch_ring<dan::kRms, 2, 8, 8, 1, 2, false, true>(q, s, scratch);
+        break;
     case 6144: e = dan::launch_ring<dan::kRms, 3, 8, 12, 3, 1, false, true>(q, s, scratch); break;
     default: e = dan::launch_ring<dan::kRms, 4, 8, 16, 4, 1, false, true>(q, s, scratch); break;
     }

@@ -826,14 +826,25 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
                 : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, false, CS>);
 }
 
+// Problems with at least this many rows per SM use 12 warps per CTA for the
+// common widths (three per scheduler: more rows in flight and fewer rows
+// per warp); smaller ones do better with 8 (measured).
+constexpr int kManyRowsPerSm = 24;
+inline bool many_rows(const RowProblem &q)
+{
+    return q.B * q.T >= (int64_t)kManyRowsPerSm * sm_count();
+}
+
 template <bool RAGGED>
 cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
 {
     switch ((q.D + 1023) / 1024) {
     case 1: return launch_ring<kLn, 4, 1, 8, 1, 1, RAGGED>(q, s);
     case 2: return launch_ring<kLn, 4, 2, 8, 1, 1, RAGGED>(q, s);
-    case 3: return launch_ring<kLn, 4, 3, 12, 1, 1, RAGGED>(q, s);
-    case 4: return launch_ring<kLn, 4, 4, 8, 1, 1, RAGGED>(q, s);
+    case 3: return many_rows(q) ? launch_ring<kLn, 4, 3, 12, 1, 1, RAGGED>(q, s)
+                                : launch_ring<kLn, 4, 3, 8, 1, 1, RAGGED>(q, s);
+    case 4: return many_rows(q) ? launch_ring<kLn, 4, 4, 12, 1, 1, RAGGED>(q, s)
+                                : launch_ring<kLn, 4, 4, 8, 1, 1, RAGGED>(q, s);
     case 5: return launch_ring<kLn, 4, 5, 8, 2, 2, RAGGED>(q, s);
     case 6: return launch_ring<kLn, 4, 6, 8, 2, 2, RAGGED>(q, s);
     case 7: return launch_ring<kLn, 4, 7, 8, 2, 2, RAGGED>(q, s);
