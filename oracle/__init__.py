@@ -19,6 +19,11 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   they are fixed by the tests only through the GPU == oracle comparison.
 * ``qk_norm_rope_epilogue``: pinned (cos=1/sin=0 and cos=0/sin=1 rotations,
   V copy, joint order, fp64 brute force).
+* ``fp8_e4m3``: pinned (every finite code decodes and re-encodes to itself,
+  midpoints round to the even code, saturation, torch's float8_e4m3fn cast
+  on the finite range, brute-force nearest code).
+* ``ln_modulate_fp8``: pinned (elementwise equal to ``fp8_e4m3`` of
+  ``ln_modulate`` times rn(1/qscale); constant rows give e4m3(shift/qscale)).
 """
 from __future__ import annotations
 
@@ -56,6 +61,8 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         lib.oracle_round_bf16.argtypes = [_P, _P, _I]
+        lib.oracle_fp8_e4m3.argtypes = [_P, _P, _I]
+        lib.oracle_ln_modulate_fp8.argtypes = [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F]
         lib.oracle_rms_modulate.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P]
         lib.oracle_gated_rms_modulate.argtypes = [_P, _P, _P, _P, _P, _P, _I, _P, _P,
                                                   _I, _I, _I, _F, _P]
@@ -203,3 +210,29 @@ def qk_norm_rope_epilogue(txt, img, H, weights, rope_txt, rope_img, eps_txt, eps
         *[_ptr(w) for w in ws], _ptr(rt), _ptr(ri), float(eps_txt), float(eps_img),
         _ptr(qo), _ptr(ko), _ptr(vo), _ptr(rs))
     return (qo, ko, vo, rs) if with_stats else (qo, ko, vo)
+
+
+def fp8_e4m3(values):
+    """fp32 values -> E4M3 codes (uint8): nearest, ties to even, saturated
+    to +-448; NaN -> 0x7F."""
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_fp8_e4m3(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def ln_modulate_fp8(x, scale, shift, qscale, eps):
+    """E4M3 codes of ln_modulate(x, scale, shift, eps) * rn(1/qscale)."""
+    x = _rows(x, "x")
+    B, T, D = x.shape
+    if D % 8:
+        raise ValueError("LayerNorm oracle needs D % 8 == 0")
+    if not (np.isfinite(qscale) and qscale > 0):
+        raise ValueError("qscale must be finite and > 0")
+    sc, ss = _vec(scale, B, D, "scale")
+    sh, hs = _vec(shift, B, D, "shift")
+    vs = _vec_stride([(sc, ss), (sh, hs)])
+    q = np.empty((B, T, D), np.uint8)
+    _load().oracle_ln_modulate_fp8(_ptr(x), _ptr(sc), _ptr(sh), vs, float(qscale), _ptr(q),
+                                   B, T, D, float(eps))
+    return q

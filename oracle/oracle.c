@@ -23,6 +23,8 @@
  *    no affine as per-element Welford and a count-weighted combine; the
  *    guide's bit-exact kernel section adds "128-thread Welford, guarded
  *    reciprocal, shfl.down fold order".
+ *  - the guide's list of fused producers: FLUX.2's LayerNorm, adaLN
+ *    modulate and static FP8 quantisation folded into one kernel.
  *  - "PR #37123 report" (Qwen-Image), implementation section 3: one
  *    epilogue doing per-head warp-reduced RMSNorm with weight, interleaved
  *    RoPE from an fp32 cos/sin cache for Q and K, a copy for V, written to
@@ -362,7 +364,64 @@ void oracle_qk_norm_rope_epilogue(const bf16_bits *q_txt, const bf16_bits *k_txt
               T_txt, q_out, k_out, v_out, rstd_out);
 }
 
+/* ------------------------------------------- LayerNorm + modulate + FP8 */
+
+/* fp32 -> FP8 E4M3 (OCP "e4m3fn": 1 sign, 4 exponent bits with bias 7, 3
+ * mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448),
+ * rounded to nearest with ties to even and saturated: a finite or infinite
+ * value of magnitude >= 448 becomes +-448.  Any NaN becomes 0x7F.
+ * Written from the format's definition: the representable values of the
+ * binade of |v| (or the subnormal range below 2^-6) are the multiples of
+ * one power-of-two quantum, so |v| / quantum is exact and rintf (round half
+ * to even in the default rounding mode) picks the nearest one. */
+static uint8_t e4m3_satfinite(float v)
+{
+    if (isnan(v)) return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const float a = fabsf(v);
+    if (a >= 448.0f) return (uint8_t)(sign | 0x7E);
+    int e = 0;
+    (void)frexpf(a, &e); /* a = m * 2^e with m in [0.5, 1); floor(log2 a) = e - 1 */
+    int ex = e - 1;
+    if (a == 0.0f || ex < -6) ex = -6; /* subnormal range: quantum 2^-9 */
+    const float quantum = ldexpf(1.0f, ex - 3);
+    const float k = rintf(a / quantum);
+    const float r = k * quantum; /* exact */
+    if (r == 0.0f) return sign;
+    if (r < ldexpf(1.0f, -6)) return (uint8_t)(sign | (uint8_t)k); /* subnormal: k/8 * 2^-6 */
+    (void)frexpf(r, &e);
+    const int biased = (e - 1) + 7;
+    const int frac = (int)(ldexpf(r, -(e - 1)) * 8.0f) - 8; /* r / 2^(e-1) = 1 + frac/8 */
+    return (uint8_t)(sign | (uint8_t)((biased << 3) | frac));
+}
+
+/* q = e4m3(rn(y * inv_s)) per element, y the bf16 result of
+ * oracle_ln_modulate, inv_s = rn(1 / qscale) for a static (per-tensor)
+ * quantisation scale qscale > 0.  "SGLang diffusion fused-op package
+ * guide", list of fused producers: FLUX.2's LayerNorm, adaLN modulate and
+ * static FP8 quantisation in one kernel.  The reciprocal multiply, the
+ * E4M3 format and the saturation are this library's readings. */
+void oracle_ln_modulate_fp8(const bf16_bits *x, const bf16_bits *scale, const bf16_bits *shift,
+                            int64_t vs, float qscale, uint8_t *q, int64_t B, int64_t T,
+                            int64_t D, float eps)
+{
+    const float inv_s = rn_div(1.0f, qscale);
+    bf16_bits *y = (bf16_bits *)malloc((size_t)(B * T * D) * sizeof(bf16_bits) + 1);
+    oracle_ln_modulate(x, scale, shift, vs, y, B, T, D, eps, NULL);
+    for (int64_t i = 0; i < B * T * D; ++i)
+        q[i] = e4m3_satfinite(rn_mul(widen(y[i]), inv_s));
+    free(y);
+}
+
 /* ------------------------------------------------------ exported helpers */
+
+/* The oracle's own fp32 -> E4M3 conversion, exposed for the tests. */
+void oracle_fp8_e4m3(const float *in, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = e4m3_satfinite(in[i]);
+}
+
 
 /* The oracle's own fp32 -> bf16 rounding, exposed so that tests can pin it
  * against an independent formulation. */

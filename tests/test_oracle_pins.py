@@ -487,3 +487,106 @@ def test_weight_single_rounding_probe(orc):
                          p["eps"], weight=bits_of(np.full(D, p["weight"])))
     expect = np.tile(np.asarray(p["expected_y_alternating"], np.float32), D // 2)
     assert np.array_equal(widen(y[0, 0]), expect)
+
+
+# ------------------------------------- LayerNorm + modulate + static FP8
+
+def e4m3_decode(code):
+    """Value of an E4M3 ("e4m3fn") code from the format's definition: sign,
+    4 exponent bits (bias 7), 3 mantissa bits, subnormals at exponent 0,
+    S.1111.111 is NaN.  Written independently of the oracle's encoder."""
+    code = int(code)
+    s = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+FINITE_CODES = [c for c in range(256) if (c & 0x7F) != 0x7F]
+
+
+def test_e4m3_decoder_matches_torch():
+    # the test's own decoder agrees with torch's float8_e4m3fn on every code
+    t = torch.tensor(list(range(256)), dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for c in range(256):
+        want = e4m3_decode(c)
+        assert (np.isnan(want) and np.isnan(t[c])) or want == t[c], c
+
+
+def test_e4m3_every_finite_code_round_trips(orc):
+    vals = np.array([e4m3_decode(c) for c in FINITE_CODES], np.float32)
+    got = orc.fp8_e4m3(vals)
+    assert list(got) == FINITE_CODES
+    assert int(got[FINITE_CODES.index(0x7E)]) == 0x7E and e4m3_decode(0x7E) == 448.0
+
+
+def test_e4m3_midpoints_round_to_even_code(orc):
+    pos = sorted((e4m3_decode(c), c) for c in range(0x7F))  # +0 .. 448
+    mids, want = [], []
+    for (a, ca), (b, cb) in zip(pos, pos[1:]):
+        mids.append((a + b) / 2)                      # exact in fp32
+        want.append(ca if ca % 2 == 0 else cb)        # ties to the even mantissa
+    got = orc.fp8_e4m3(np.array(mids, np.float32))
+    assert list(got) == want
+    assert list(orc.fp8_e4m3(-np.array(mids, np.float32))) == [w | 0x80 for w in want]
+
+
+def test_e4m3_saturation_and_specials(orc):
+    v = np.array([448.0, 449.0, 463.9, 464.0, 480.0, 1e30, np.inf, -500.0, -np.inf,
+                  np.nan, 0.0, -0.0, 2.0 ** -10, 2.0 ** -9, 2.0 ** -6 - 2.0 ** -10], np.float32)
+    got = [int(c) for c in orc.fp8_e4m3(v)]
+    assert got[:9] == [0x7E] * 7 + [0xFE, 0xFE]
+    assert got[9] == 0x7F and got[10] == 0x00 and got[11] == 0x80
+    assert got[12] == 0x00            # half the smallest subnormal: tie to even (zero)
+    assert got[13] == 0x01            # the smallest subnormal
+    assert got[14] == 0x08            # 2^-6 - 2^-10 is the midpoint 7.5/8: rounds to even 8/8
+
+
+def test_e4m3_matches_torch_cast_in_range(orc):
+    rng = np.random.default_rng(21)
+    v = np.concatenate([rng.normal(0, 1, 20000), rng.normal(0, 100, 20000),
+                        rng.uniform(-447, 447, 20000), rng.normal(0, 2.0 ** -7, 20000)])
+    v = v.astype(np.float32)
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.fp8_e4m3(v), want)
+
+
+def test_e4m3_brute_force_nearest(orc):
+    rng = np.random.default_rng(22)
+    v = (rng.normal(0, 30, 3000) * rng.choice([1.0, 2.0 ** -8], 3000)).astype(np.float32)
+    vals = np.array([e4m3_decode(c) for c in FINITE_CODES])
+    got = orc.fp8_e4m3(v)
+    for x, g in zip(v.astype(np.float64), got):
+        d = np.abs(vals - min(max(x, -448.0), 448.0))
+        best = [FINITE_CODES[i] for i in np.flatnonzero(d == d.min())]
+        best = [c for c in best if (c & 0x80) == (0x80 if np.signbit(x) else 0)] or best
+        want = min(best, key=lambda c: (c & 1, c))  # a tie goes to the even mantissa
+        assert int(g) == want, (x, int(g), want)
+
+
+def test_ln_fp8_constant_rows_quantise_shift(orc):
+    B, T, D = 2, 5, 3072
+    c = widen(synth.normal_bf16((B, T), 31, 2.0))
+    x = bits_of(np.broadcast_to(c[..., None], (B, T, D)))
+    scale = synth.normal_bf16((B, D), 32, 0.2)
+    shift = synth.normal_bf16((B, D), 33, 3.0)
+    qscale = 0.0625  # 1/qscale = 16 exactly
+    q = orc.ln_modulate_fp8(x, scale, shift, qscale, EPS)
+    want = torch.from_numpy(widen(shift) * np.float32(16.0)).to(torch.float8_e4m3fn)
+    want = want.view(torch.uint8).numpy()
+    assert np.array_equal(q, np.broadcast_to(want[:, None, :], (B, T, D)))
+
+
+def test_ln_fp8_is_quantised_ln_modulate(orc):
+    x = synth.outlier_rows_bf16((1, 64, 4096), 34, synth.SEED_OUTLIER)
+    scale = synth.normal_bf16((1, 4096), 35, 0.2)
+    shift = synth.normal_bf16((1, 4096), 36, 0.2)
+    for qscale in (1.0, 0.02, 3.0):
+        inv = np.float32(1.0) / np.float32(qscale)
+        y = orc.ln_modulate(x, scale, shift, EPS)
+        want = torch.from_numpy(widen(y) * inv).clamp(-448, 448).to(torch.float8_e4m3fn)
+        assert np.array_equal(orc.ln_modulate_fp8(x, scale, shift, qscale, EPS),
+                              want.view(torch.uint8).numpy())
