@@ -143,6 +143,20 @@ int validate_ln(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
     return check_buffers(ins, 3, outs, 1, inplace, 1);
 }
 
+int validate_ln_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift, int64_t vs,
+                    float qscale, const uint8_t *q, int64_t B, int64_t T, int64_t D, float eps,
+                    bool *empty)
+{
+    int st = check_rows(B, T, D, eps, vs, ln_d_ok(D));
+    if (st == DAN_OK && !(std::isfinite(qscale) && qscale > 0.0f)) st = DAN_EINVAL;
+    *empty = (st == DAN_OK && B * T == 0);
+    if (st != DAN_OK || *empty) return st;
+    Buf ins[3] = {{x, span(x, B * T * D * 2)}, {scale, span(scale, vec_bytes(B, D, vs))},
+                  {shift, span(shift, vec_bytes(B, D, vs))}};
+    Buf outs[1] = {{q, span(q, B * T * D)}}; // one byte per element; no in-place form
+    return check_buffers(ins, 3, outs, 1, nullptr, 0);
+}
+
 int validate_qk(const dan_bf16 *const qkv[2][3], const int64_t Ts[2], const int64_t strides[2],
                 int64_t heads, int64_t head_dim, const dan_bf16 *const w[4],
                 const float *const rope[2], const float eps[2], const dan_bf16 *const outs_p[3],
@@ -357,6 +371,28 @@ int dan_ln_modulate(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *sh
     dan::RowProblem p{x, nullptr, nullptr, nullptr, scale, shift, vec_bstride, y, nullptr,
                       B, T, D, eps};
     return launched(dan::launch_ln_modulate(p, static_cast<cudaStream_t>(stream)));
+}
+
+int dan_can_use_ln_modulate_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
+                                int64_t vec_bstride, float qscale, const uint8_t *q, int64_t B,
+                                int64_t T, int64_t D, float eps)
+{
+    bool empty;
+    return validate_ln_fp8(x, scale, shift, vec_bstride, qscale, q, B, T, D, eps, &empty);
+}
+
+int dan_ln_modulate_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
+                        int64_t vec_bstride, float qscale, uint8_t *q, int64_t B, int64_t T,
+                        int64_t D, float eps, void *stream)
+{
+    bool empty;
+    const int st = validate_ln_fp8(x, scale, shift, vec_bstride, qscale, q, B, T, D, eps, &empty);
+    if (st != DAN_OK || empty) return st;
+    dan::RowProblem p{x, nullptr, nullptr, nullptr, scale, shift, vec_bstride, nullptr, nullptr,
+                      B, T, D, eps};
+    p.q = q;
+    p.qinv = 1.0f / qscale; // one IEEE division on the host: rn(1 / qscale)
+    return launched(dan::launch_ln_modulate_fp8(p, static_cast<cudaStream_t>(stream)));
 }
 
 int dan_can_use_qk_norm_rope_epilogue(

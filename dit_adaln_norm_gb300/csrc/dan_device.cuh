@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,6 +64,20 @@ __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v)
     asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
                  "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// Streaming 8-byte global store.
+__device__ __forceinline__ void st_stream8(uint2 *p, const uint2 &v)
+{
+    asm volatile("st.global.L1::no_allocate.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y)
+                 : "memory");
+}
+
+// Two fp32 values to FP8 E4M3 codes (round to nearest even, saturated to the
+// largest finite value), v.x in the low byte.
+__device__ __forceinline__ uint32_t fp8x2_e4m3(float2 v)
+{
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
 }
 
 // Asynchronous 16-byte global -> shared copy (bypassing L1), and the wait

@@ -20,6 +20,8 @@ struct RowProblem {
     void *r_out; // gated residual output, or nullptr
     int64_t B, T, D;
     float eps;
+    void *q = nullptr;  // E4M3 output (LayerNorm + FP8), or nullptr
+    float qinv = 0.0f;  // rn(1 / qscale) (LayerNorm + FP8)
 };
 
 struct QkProblem {
@@ -58,6 +60,7 @@ cudaError_t launch_overlapped(void (*fn)(KArgs...), int grid, int block, int sme
 cudaError_t launch_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_gated_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_ln_modulate(const RowProblem &p, cudaStream_t s);
+cudaError_t launch_ln_modulate_fp8(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &p, cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).

@@ -53,6 +53,8 @@ struct RowParams {
     const uint4 *weight;
     uint4 *y;
     uint4 *r_out;
+    uint2 *q8;   // E4M3 output, 8 codes per 16-byte input fragment (LN + FP8 only)
+    float qinv;  // rn(1 / qscale) (LN + FP8 only)
     int64_t rows;
     int64_t T;
     int64_t vs8; // batch stride of the vectors in 16-byte fragments
@@ -231,6 +233,21 @@ __device__ __forceinline__ void modulate_store(uint4 *dst, const float (&t)[8], 
     for (int w = 0; w < 4; ++w)
         set_word(out, w, modulate_word(pack_bf16(t[2 * w], t[2 * w + 1]), word(o, w), word(sh, w)));
     st_stream(dst, out);
+}
+
+// The same modulate, then the static FP8 quantisation of each bf16 result:
+// q = e4m3(rn(y * qinv)), nearest even, saturated to +-448; eight codes (8 B)
+// per fragment.
+__device__ __forceinline__ void modulate_store_fp8(uint2 *dst, const float (&t)[8], const uint4 &o,
+                                                   const uint4 &sh, float2 qinv2)
+{
+    uint32_t codes[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t y = modulate_word(pack_bf16(t[2 * w], t[2 * w + 1]), word(o, w), word(sh, w));
+        codes[w] = fp8x2_e4m3(mul2(wide2(y), qinv2));
+    }
+    st_stream8(dst, make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16)));
 }
 
 // Normalise, modulate and store the logical warps j0 .. j0+LWW-1 of a row
@@ -454,8 +471,9 @@ __device__ __forceinline__ void ln_final(const Welford (&W)[4], float &mean, flo
     }
 }
 
-// Normalise, modulate and store the logical warps r + TW*m of a row.
-template <int FPT, int J, int TW, bool RAGGED, bool STAGED>
+// Normalise, modulate and store (FP8: quantise and store) the logical warps
+// r + TW*m of a row.
+template <int FPT, int J, int TW, bool RAGGED, bool STAGED, bool FP8>
 __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, float mean, float m2,
                                          const RowParams &p, int64_t row, int64_t bidx,
                                          const uint4 *s_vec, int lane)
@@ -464,7 +482,15 @@ __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, flo
     const int F = p.F;
     const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
     const float2 mean2 = dup2(mean);
-    uint4 *y = p.y + row * F;
+    uint4 *y = FP8 ? nullptr : p.y + row * F;
+    uint2 *q8 = FP8 ? p.q8 + row * F : nullptr;
+    const float2 qinv2 = dup2(p.qinv);
+    auto out = [&](int f, const float (&t)[8]) {
+        const uint4 o = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 0);
+        const uint4 sh = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 1);
+        if (FP8) modulate_store_fp8(q8 + f, t, o, sh, qinv2);
+        else modulate_store(y + f, t, o, sh);
+    };
     if (!RAGGED && J >= 2) { // pairs across logical warps, as in ln_states
 #pragma unroll
         for (int q = 0; q < J / 2; ++q)
@@ -480,10 +506,8 @@ __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, flo
                     t0[e] = t2.x;
                     t1[e] = t2.y;
                 }
-                modulate_store(y + f0, t0, vec_frag<NV, STAGED>(p, s_vec, bidx, f0, 0),
-                               vec_frag<NV, STAGED>(p, s_vec, bidx, f0, 1));
-                modulate_store(y + f1, t1, vec_frag<NV, STAGED>(p, s_vec, bidx, f1, 0),
-                               vec_frag<NV, STAGED>(p, s_vec, bidx, f1, 1));
+                out(f0, t0);
+                out(f1, t1);
             }
     } else { // neighbouring elements of one logical warp
 #pragma unroll
@@ -499,15 +523,14 @@ __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, flo
                     t[e] = t2.x;
                     t[e + 1] = t2.y;
                 }
-                modulate_store(y + f, t, vec_frag<NV, STAGED>(p, s_vec, bidx, f, 0),
-                               vec_frag<NV, STAGED>(p, s_vec, bidx, f, 1));
+                out(f, t);
             }
     }
 }
 
 // ------------------------------------------------------- the row kernel
 
-enum RowKind { kRms = 0, kGated = 1, kLn = 2 };
+enum RowKind { kRms = 0, kGated = 1, kLn = 2, kLnFp8 = 3 };
 
 template <int KIND>
 struct RowShape {
@@ -551,10 +574,11 @@ __global__ void __launch_bounds__(32 * NW, 1)
     using Pipe = WarpPipe<SPC>;
     using Lay = RowLayout<KIND, NW, TW, SPC>;
     constexpr int NIN = Shape::NIN, NV = Shape::NV, NT = Lay::NT;
-    constexpr int LWW = KIND == kLn ? 1 : LW / TW; // RMS logical warps per warp
-    constexpr int J = KIND == kLn ? 4 / TW : 1;     // LayerNorm logical warps per warp
+    constexpr bool LN = KIND == kLn || KIND == kLnFp8;
+    constexpr int LWW = LN ? 1 : LW / TW; // RMS logical warps per warp
+    constexpr int J = LN ? 4 / TW : 1;     // LayerNorm logical warps per warp
     static_assert(NW % TW == 0, "teams of TW warps");
-    static_assert(KIND == kLn ? (4 % TW == 0) : (LW % TW == 0), "TW divides the logical warps");
+    static_assert(LN ? (4 % TW == 0) : (LW % TW == 0), "TW divides the logical warps");
     const int F = p.F;
     const unsigned row_bytes = (unsigned)F * 16u;
 
@@ -650,7 +674,7 @@ __global__ void __launch_bounds__(32 * NW, 1)
             if (lane == 0) mbar_arrive(done_bar + team);
             return mbar_wait(done_bar + team, (unsigned)i & 1u, p.limit_ns);
         };
-        if (KIND == kLn) {
+        if (LN) {
             float x[J][FPT][8];
 #pragma unroll
             for (int m = 0; m < J; ++m)
@@ -689,7 +713,8 @@ __global__ void __launch_bounds__(32 * NW, 1)
                 for (int m = 0; m < 4; ++m) all[m] = Welford{xch[3 * m], xch[3 * m + 1], xch[3 * m + 2]};
             float mean, m2;
             ln_final<RAGGED>(all, mean, m2);
-            ln_store<FPT, J, TW, RAGGED, STAGED>(x, r, mean, m2, p, row, bidx, s_vec, lane);
+            ln_store<FPT, J, TW, RAGGED, STAGED, KIND == kLnFp8>(x, r, mean, m2, p, row, bidx,
+                                                                 s_vec, lane);
         } else {
             float x[LWW][8][8];
             const int j0 = r * LWW;
@@ -761,6 +786,8 @@ RowParams make_params(const RowProblem &q)
     p.weight = static_cast<const uint4 *>(q.weight);
     p.y = static_cast<uint4 *>(q.y);
     p.r_out = static_cast<uint4 *>(q.r_out);
+    p.q8 = static_cast<uint2 *>(q.q);
+    p.qinv = q.qinv;
     p.rows = q.B * q.T;
     p.T = q.T;
     p.vs8 = q.vs / 8;
@@ -794,7 +821,8 @@ int ring_smem(const RowProblem &q, RowParams &p)
     using Lay = RowLayout<KIND, NW, TW, SPC>;
     const int64_t row_bytes = q.D * 2;
     const int64_t fixed = Lay::slots_bytes((int)(q.D / 8)) +
-                          (KIND != kLn && q.weight ? row_bytes : 0) + Lay::tail_bytes;
+                          ((KIND == kRms || KIND == kGated) && q.weight ? row_bytes : 0) +
+                          Lay::tail_bytes;
     const int64_t vec_bytes = q.B * Shape::NV * row_bytes;
     const int64_t room = (int64_t)max_smem_optin() - fixed;
     p.Bs = (vec_bytes <= kStageBudget && vec_bytes <= room) ? (int)q.B : 0;
@@ -809,7 +837,7 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
 {
     RowParams p = make_params(q);
     p.cta_status = cta_status;
-    const bool has_w = KIND != kLn && q.weight != nullptr;
+    const bool has_w = (KIND == kRms || KIND == kGated) && q.weight != nullptr;
     const int smem = ring_smem<KIND, NW, TW, SPC>(q, p);
     const int grid = (int)(p.rows < sm_count() ? p.rows : sm_count());
     const InvTable2 inv = inv_table();
@@ -819,9 +847,11 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
         return launch_overlapped(fn, grid, 32 * NW, smem, s, p, inv);
     };
     constexpr bool CS = CTA_STATUS;
-    if (has_w)
-        return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, true, CS>)
-                    : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, false, CS>);
+    if constexpr (KIND == kRms || KIND == kGated) {
+        if (has_w)
+            return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, true, CS>)
+                        : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, false, CS>);
+    }
     return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, true, CS>)
                 : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, false, CS>);
 }
@@ -835,20 +865,20 @@ inline bool many_rows(const RowProblem &q)
     return q.B * q.T >= (int64_t)kManyRowsPerSm * sm_count();
 }
 
-template <bool RAGGED>
+template <int KIND, bool RAGGED>
 cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
 {
     switch ((q.D + 1023) / 1024) {
-    case 1: return launch_ring<kLn, 4, 1, 8, 1, 1, RAGGED>(q, s);
-    case 2: return launch_ring<kLn, 4, 2, 8, 1, 1, RAGGED>(q, s);
-    case 3: return many_rows(q) ? launch_ring<kLn, 4, 3, 12, 1, 1, RAGGED>(q, s)
-                                : launch_ring<kLn, 4, 3, 8, 1, 1, RAGGED>(q, s);
-    case 4: return many_rows(q) ? launch_ring<kLn, 4, 4, 12, 1, 1, RAGGED>(q, s)
-                                : launch_ring<kLn, 4, 4, 8, 1, 1, RAGGED>(q, s);
-    case 5: return launch_ring<kLn, 4, 5, 8, 2, 2, RAGGED>(q, s);
-    case 6: return launch_ring<kLn, 4, 6, 8, 2, 2, RAGGED>(q, s);
-    case 7: return launch_ring<kLn, 4, 7, 8, 2, 2, RAGGED>(q, s);
-    default: return launch_ring<kLn, 4, 8, 8, 2, 2, RAGGED>(q, s);
+    case 1: return launch_ring<KIND, 4, 1, 8, 1, 1, RAGGED>(q, s);
+    case 2: return launch_ring<KIND, 4, 2, 8, 1, 1, RAGGED>(q, s);
+    case 3: return many_rows(q) ? launch_ring<KIND, 4, 3, 12, 1, 1, RAGGED>(q, s)
+                                : launch_ring<KIND, 4, 3, 8, 1, 1, RAGGED>(q, s);
+    case 4: return many_rows(q) ? launch_ring<KIND, 4, 4, 12, 1, 1, RAGGED>(q, s)
+                                : launch_ring<KIND, 4, 4, 8, 1, 1, RAGGED>(q, s);
+    case 5: return launch_ring<KIND, 4, 5, 8, 2, 2, RAGGED>(q, s);
+    case 6: return launch_ring<KIND, 4, 6, 8, 2, 2, RAGGED>(q, s);
+    case 7: return launch_ring<KIND, 4, 7, 8, 2, 2, RAGGED>(q, s);
+    default: return launch_ring<KIND, 4, 8, 8, 2, 2, RAGGED>(q, s);
     }
 }
 

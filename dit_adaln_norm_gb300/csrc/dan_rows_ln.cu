@@ -27,7 +27,7 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s)
 
 cudaError_t launch_ln_modulate(const RowProblem &q, cudaStream_t s)
 {
-    return (q.D % 1024) ? launch_ln_fpt<true>(q, s) : launch_ln_fpt<false>(q, s);
+    return (q.D % 1024) ? launch_ln_fpt<kLn, true>(q, s) : launch_ln_fpt<kLn, false>(q, s);
 }
 
 } // namespace dan

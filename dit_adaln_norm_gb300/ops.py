@@ -33,6 +33,8 @@ _SIGS = {
     "dan_can_use_gated_rms_modulate": [_P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F],
     "dan_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F, _P],
     "dan_can_use_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F],
+    "dan_ln_modulate_fp8": [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F, _P],
+    "dan_can_use_ln_modulate_fp8": [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F],
     "dan_qk_norm_rope_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
                                   _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P],
     "dan_can_use_qk_norm_rope_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
@@ -80,9 +82,9 @@ def status_string(status: int) -> str:
 
 
 def device_status() -> int:
-    """Read and clear the current device's status word (bit 1: a consumer
-    gave up waiting for a row, 2: the producer for a slot, 4: the producer
-    for its own copies).  Synchronous; 0 when every wait completed."""
+    """Read and clear the current device's status word (bit 1: a warp gave
+    up waiting for a row it requested, 4: it then also gave up on its other
+    copies in flight).  Synchronous; 0 when every wait completed."""
     v = ctypes.c_uint(0)
     _check(load().dan_get_device_status(ctypes.byref(v)), "dan_get_device_status")
     return v.value
@@ -183,6 +185,21 @@ def ln_modulate(x, scale, shift, eps: float, out=None):
     _check(load().dan_ln_modulate(_ptr(x), _ptr(scale), _ptr(shift), vs, _ptr(y), B, T, D,
                                   float(eps), _stream()), "dan_ln_modulate")
     return y
+
+
+def ln_modulate_fp8(x, scale, shift, qscale: float, eps: float, out=None):
+    """q = e4m3(ln_modulate(x, scale, shift, eps) * rn(1/qscale)) as a
+    torch.uint8 [B, T, D] tensor of E4M3 codes (view it as
+    torch.float8_e4m3fn for an FP8 GEMM)."""
+    B, T, D = _rows(x, "x")
+    vs = _vectors(B, D, [("scale", scale), ("shift", shift)])
+    q = torch.empty((B, T, D), dtype=torch.uint8, device=x.device) if out is None else out
+    if q.dtype != torch.uint8 or not q.is_cuda or tuple(q.shape) != (B, T, D) or not q.is_contiguous():
+        raise ValueError("out: expected a contiguous CUDA uint8 [B, T, D] tensor")
+    _check(load().dan_ln_modulate_fp8(_ptr(x), _ptr(scale), _ptr(shift), vs, float(qscale),
+                                      _ptr(q), B, T, D, float(eps), _stream()),
+           "dan_ln_modulate_fp8")
+    return q
 
 
 def _qkv(views, name, heads):

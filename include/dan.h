@@ -1,9 +1,10 @@
 /*
  * dan.h -- C ABI of the GB300 (sm_103a) fused adaLN norm+modulate kernels.
  *
- * Four operations, each a single kernel launch on the caller's stream:
+ * Five operations, each a single kernel launch on the caller's stream:
  *
  *   dan_ln_modulate         y = bf16(LayerNorm(x) * (1 + scale) + shift)
+ *   dan_ln_modulate_fp8     q = e4m3(y * rn(1/qscale)), y as dan_ln_modulate
  *   dan_rms_modulate        y = bf16(RMSNorm(x) [* w] * (1 + scale) + shift)
  *   dan_gated_rms_modulate  r' = bf16(r + bf16(gate * h)); y = rms_modulate(r')
  *   dan_qk_norm_rope_epilogue  per-head RMSNorm + interleaved RoPE of Q and K,
@@ -171,6 +172,26 @@ int dan_ln_modulate(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *sh
 int dan_can_use_ln_modulate(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
                             int64_t vec_bstride, const dan_bf16 *y, int64_t B, int64_t T,
                             int64_t D, float eps);
+
+/* ------------------------------------------- LayerNorm + modulate + FP8
+ * "SGLang diffusion fused-op package guide", list of fused producers:
+ * FLUX.2's LayerNorm, adaLN modulate and static FP8 quantisation folded
+ * into one kernel, which feeds an FP8 GEMM.  Per element
+ *   q = e4m3(rn(y * rn(1 / qscale)))
+ * with y the bf16 result dan_ln_modulate would return (same arguments, same
+ * bits) and e4m3 the OCP E4M3 ("e4m3fn") code: round to nearest, ties to
+ * even, values of magnitude >= 448 (and infinities) saturated to +-448, NaN
+ * to a NaN code.  qscale is the static per-tensor scale (finite, > 0);
+ * rn(1/qscale) is one IEEE division on the host.  q is [B, T, D] bytes,
+ * contiguous, 16-byte aligned, and may not overlap any input (no in-place
+ * form).  Supported D as for dan_ln_modulate.  Returns DAN_EINVAL for a bad
+ * qscale, otherwise as dan_ln_modulate. */
+int dan_ln_modulate_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
+                        int64_t vec_bstride, float qscale, uint8_t *q, int64_t B, int64_t T,
+                        int64_t D, float eps, void *stream);
+int dan_can_use_ln_modulate_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
+                                int64_t vec_bstride, float qscale, const uint8_t *q, int64_t B,
+                                int64_t T, int64_t D, float eps);
 
 /* ------------------------------------------- QK-RMSNorm + RoPE epilogue
  * Two token streams (text, then image), each given as three row-strided

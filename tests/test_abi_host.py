@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = ops.declared_symbols()
-    assert len(names) == 12
+    assert len(names) == 14
     for n in names:
         assert hasattr(lib, n), n
 
@@ -90,6 +90,20 @@ def test_ln_validation(lib):
         assert f(D=D, vs=max(D, 8)) == EUNSUP, D
     assert f(y=X) == OK and f(y=X + 16) == EALIAS
     assert f(B=2, vs=6 * 3072) == OK and f(B=2, vs=3076) == EALIGN
+
+
+def test_ln_fp8_validation(lib):
+    def f(x=X, sc=SC, sh=SH, vs=4096, qs=0.5, q=Y, B=1, T=4216, D=4096, eps=EPS):
+        return lib.dan_can_use_ln_modulate_fp8(x, sc, sh, vs, qs, q, B, T, D, eps)
+
+    assert f() == OK and f(D=3072, vs=3072) == OK
+    for qs in (0.0, -1.0, float("inf"), float("nan")):
+        assert f(qs=qs) == EINVAL
+    assert f(q=None) == EINVAL and f(q=Y + 8) == EALIGN
+    assert f(q=X) == EALIAS                      # no in-place form
+    assert f(q=X + 4216 * 4096 * 2) == OK        # right after x
+    assert f(D=12, vs=16) == EUNSUP
+    assert f(T=0, x=None, q=None) == OK
 
 
 def test_qk_validation(lib):

@@ -307,3 +307,51 @@ def test_signed_zeros_through_the_modulate_chain():
     gr, gy = ops.gated_rms_modulate(to_dev(r), to_dev(x), to_dev(g), to_dev(sc), to_dev(sh), EPS)
     assert_bits_equal(from_dev(gr), wr, "signed zeros gated r'")
     assert_bits_equal(from_dev(gy), wy, "signed zeros gated y")
+
+
+# ------------------------------------------------ LayerNorm + modulate + FP8
+
+def run_ln_fp8(B, T, D, seed, qscale, outliers=True, chunks=6, x_bits=None):
+    if x_bits is not None:
+        x = x_bits
+    elif outliers:
+        x = synth.outlier_rows_bf16((B, T, D), seed, synth.SEED_OUTLIER)
+    else:
+        x = synth.normal_bf16((B, T, D), seed)
+    (sc, sh), (dsc, dsh) = adaln(B, D, 2, seed + 1, 0.2, chunks)
+    total = B * T * D
+    buf = torch.full((total + 2 * 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    q = buf[4096:4096 + total].view(B, T, D)
+    ops.ln_modulate_fp8(to_dev(x), dsc, dsh, qscale, EPS, out=q)
+    torch.cuda.synchronize()
+    assert bool((buf[:4096] == 0xA5).all()) and bool((buf[4096 + total:] == 0xA5).all())
+    want = oracle.ln_modulate_fp8(x, sc, sh, qscale, EPS)
+    got = q.cpu().numpy()
+    nan = lambda c: (c & 0x7F) == 0x7F
+    same = (got == want) | (nan(got) & nan(want))
+    assert same.all(), (f"ln_fp8 B={B} T={T} D={D} qscale={qscale}: {int((~same).sum())} codes "
+                        f"differ, first at {np.argwhere(~same)[0]}")
+
+
+@pytest.mark.parametrize("D", [8, 1040, 2048, 3072, 4096, 5000, 8192])
+def test_ln_fp8_small(D):
+    run_ln_fp8(2, 19, D, 400 + D, 0.05)
+
+
+@pytest.mark.parametrize("qscale", [1.0, 0.0078125, 0.003, 7.5])
+def test_ln_fp8_scales_and_saturation(qscale):
+    # small scales push most codes into saturation at +-448
+    run_ln_fp8(1, 257, 3072, 410, qscale)
+
+
+def test_ln_fp8_extreme_rows():
+    D = 1024
+    rows = [np.zeros(D), np.full(D, 3.0), np.where(np.arange(D) % 2 == 0, 1e4, -1e4),
+            np.linspace(-1e-30, 1e-30, D), np.random.default_rng(411).normal(0, 50, D)]
+    x = np.stack([synth.to_bf16_bits(np.asarray(r, np.float32)) for r in rows])[None]
+    run_ln_fp8(1, len(rows), D, 412, 0.1, x_bits=x)
+
+
+def test_ln_fp8_metric_shape_and_cfg_batch():
+    run_ln_fp8(1, 4216, 4096, synth.SEED_X, 0.05)
+    run_ln_fp8(2, 1140, 4096, synth.SEED_X + 1, 0.05)
