@@ -19,6 +19,8 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   they are fixed by the tests only through the GPU == oracle comparison.
 * ``qk_norm_rope_epilogue``: pinned (cos=1/sin=0 and cos=0/sin=1 rotations,
   V copy, joint order, fp64 brute force).
+* ``gated_ln_modulate``: pinned (r' against an independent elementwise
+  formula, gate = 0 and the composition with ``ln_modulate`` of r').
 * ``fp8_e4m3``: pinned (every finite code decodes and re-encodes to itself,
   midpoints round to the even code, saturation, torch's float8_e4m3fn cast
   on the finite range, brute-force nearest code).
@@ -62,6 +64,8 @@ def _load():
         lib = ctypes.CDLL(build())
         lib.oracle_round_bf16.argtypes = [_P, _P, _I]
         lib.oracle_fp8_e4m3.argtypes = [_P, _P, _I]
+        lib.oracle_gated_ln_modulate.argtypes = [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F,
+                                                 _P]
         lib.oracle_ln_modulate_fp8.argtypes = [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F]
         lib.oracle_rms_modulate.argtypes = [_P, _P, _P, _P, _I, _P, _I, _I, _I, _F, _P]
         lib.oracle_gated_rms_modulate.argtypes = [_P, _P, _P, _P, _P, _P, _I, _P, _P,
@@ -236,3 +240,22 @@ def ln_modulate_fp8(x, scale, shift, qscale, eps):
     _load().oracle_ln_modulate_fp8(_ptr(x), _ptr(sc), _ptr(sh), vs, float(qscale), _ptr(q),
                                    B, T, D, float(eps))
     return q
+
+
+def gated_ln_modulate(r, h, gate, scale, shift, eps, with_stats=False):
+    """r' = bf16(r + bf16(gate * h)); y = ln_modulate(r').  Returns (r', y)."""
+    r = _rows(r, "r")
+    h = _rows(h, "h")
+    B, T, D = r.shape
+    if h.shape != r.shape or D % 8:
+        raise ValueError("gated LayerNorm oracle: r, h must match and D % 8 == 0")
+    g, gs = _vec(gate, B, D, "gate")
+    sc, ss = _vec(scale, B, D, "scale")
+    sh, hs = _vec(shift, B, D, "shift")
+    vs = _vec_stride([(g, gs), (sc, ss), (sh, hs)])
+    r_out = np.empty_like(r)
+    y = np.empty_like(r)
+    st = np.empty((B * T, 3), np.float32) if with_stats else None
+    _load().oracle_gated_ln_modulate(_ptr(r), _ptr(h), _ptr(g), _ptr(sc), _ptr(sh), vs,
+                                     _ptr(r_out), _ptr(y), B, T, D, float(eps), _ptr(st))
+    return (r_out, y, st) if with_stats else (r_out, y)

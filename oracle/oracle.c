@@ -256,8 +256,27 @@ static welford ln_statistics(const float *x, int64_t D)
     return warp[0];
 }
 
-/* y = bf16(LN(x) * (1+scale) + shift), LayerNorm without affine;
- * n = bf(rn(rn(x - mean) * rstd)), rstd = rn(1/rn(sqrt(rn(rn(m2/D) + eps)))).
+/* One LayerNorm + modulate row: n = bf(rn(rn(x - mean) * rstd)),
+ * rstd = rn(1/rn(sqrt(rn(rn(m2/D) + eps)))), y = modulate(n, scale, shift).
+ * stats (nullable): {mean, m2, rstd}. */
+static void ln_row(const float *xrow, const bf16_bits *scale, const bf16_bits *shift,
+                   bf16_bits *y, int64_t D, float eps, float *stats)
+{
+    welford st = ln_statistics(xrow, D);
+    float var = rn_div(st.m2, (float)D);
+    float rstd = defined_rsqrt(rn_add(var, eps));
+    for (int64_t j = 0; j < D; ++j) {
+        float n = bf(rn_mul(rn_sub(xrow[j], st.mean), rstd));
+        y[j] = modulate(n, widen(scale[j]), widen(shift[j]));
+    }
+    if (stats) {
+        stats[0] = st.mean;
+        stats[1] = st.m2;
+        stats[2] = rstd;
+    }
+}
+
+/* y = bf16(LN(x) * (1+scale) + shift), LayerNorm without affine.
  * stats (nullable): per row {mean, m2, rstd}.  Requires D % 8 == 0. */
 void oracle_ln_modulate(const bf16_bits *x, const bf16_bits *scale, const bf16_bits *shift,
                         int64_t vs, bf16_bits *y, int64_t B, int64_t T, int64_t D, float eps,
@@ -268,18 +287,33 @@ void oracle_ln_modulate(const bf16_bits *x, const bf16_bits *scale, const bf16_b
         int64_t b = r / T;
         for (int64_t j = 0; j < D; ++j)
             xrow[j] = widen(x[r * D + j]);
-        welford st = ln_statistics(xrow, D);
-        float var = rn_div(st.m2, (float)D);
-        float rstd = defined_rsqrt(rn_add(var, eps));
+        ln_row(xrow, scale + b * vs, shift + b * vs, y + r * D, D, eps,
+               stats ? stats + 3 * r : NULL);
+    }
+    free(xrow);
+}
+
+/* The gated residual form with LayerNorm: r' = bf(rn(r + bf(rn(gate * h))))
+ * is stored, then y = the LayerNorm + modulate row of r'.  The guide's
+ * residual variant (round(gate*update), then round(residual + that), the
+ * rounded result fed to the same faithful norm) with the LayerNorm of the
+ * FLUX pages in place of RMSNorm.  gate, scale, shift share vs. */
+void oracle_gated_ln_modulate(const bf16_bits *r, const bf16_bits *h, const bf16_bits *gate,
+                              const bf16_bits *scale, const bf16_bits *shift, int64_t vs,
+                              bf16_bits *r_out, bf16_bits *y, int64_t B, int64_t T, int64_t D,
+                              float eps, float *stats)
+{
+    float *xrow = (float *)malloc((size_t)D * sizeof(float));
+    for (int64_t row = 0; row < B * T; ++row) {
+        int64_t b = row / T;
         for (int64_t j = 0; j < D; ++j) {
-            float n = bf(rn_mul(rn_sub(xrow[j], st.mean), rstd));
-            y[r * D + j] = modulate(n, widen(scale[b * vs + j]), widen(shift[b * vs + j]));
+            float gh = bf(rn_mul(widen(gate[b * vs + j]), widen(h[row * D + j])));
+            bf16_bits rp = narrow(rn_add(widen(r[row * D + j]), gh));
+            r_out[row * D + j] = rp;
+            xrow[j] = widen(rp);
         }
-        if (stats) {
-            stats[3 * r + 0] = st.mean;
-            stats[3 * r + 1] = st.m2;
-            stats[3 * r + 2] = rstd;
-        }
+        ln_row(xrow, scale + b * vs, shift + b * vs, y + row * D, D, eps,
+               stats ? stats + 3 * row : NULL);
     }
     free(xrow);
 }

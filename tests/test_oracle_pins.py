@@ -590,3 +590,33 @@ def test_ln_fp8_is_quantised_ln_modulate(orc):
         want = torch.from_numpy(widen(y) * inv).clamp(-448, 448).to(torch.float8_e4m3fn)
         assert np.array_equal(orc.ln_modulate_fp8(x, scale, shift, qscale, EPS),
                               want.view(torch.uint8).numpy())
+
+
+# ---------------------------------------------- gated residual + LayerNorm
+
+def test_gated_ln_residual_and_composition(orc):
+    B, T, D = 2, 9, 3072
+    r = synth.normal_bf16((B, T, D), 40)
+    h = synth.normal_bf16((B, T, D), 41)
+    gate, scale, shift = synth.adaln_vectors(B, D, 3, 42, 0.1)
+    r_out, y = orc.gated_ln_modulate(r, h, gate, scale, shift, EPS)
+    # r' independently: round(gate*h) then round(r + that), in torch bf16 ops
+    tg = torch.from_numpy(widen(gate)[:, None, :]).to(torch.bfloat16)
+    th = torch.from_numpy(widen(h)).to(torch.bfloat16)
+    tr = torch.from_numpy(widen(r)).to(torch.bfloat16)
+    want_r = (tr + tg * th).float().numpy()
+    assert np.array_equal(widen(r_out), want_r)
+    # y is the LayerNorm + modulate of r'
+    assert np.array_equal(y, orc.ln_modulate(r_out, scale, shift, EPS))
+
+
+def test_gated_ln_zero_gate_is_ln_of_residual(orc):
+    B, T, D = 1, 5, 1040
+    r = synth.outlier_rows_bf16((B, T, D), 43, synth.SEED_OUTLIER)
+    h = synth.normal_bf16((B, T, D), 44)
+    zeros = vec(B, D, 0.0)
+    scale = synth.normal_bf16((B, D), 45, 0.2)
+    shift = synth.normal_bf16((B, D), 46, 0.2)
+    r_out, y = orc.gated_ln_modulate(r, h, zeros, scale, shift, EPS)
+    assert np.array_equal(r_out, r)
+    assert np.array_equal(y, orc.ln_modulate(r, scale, shift, EPS))
