@@ -642,6 +642,8 @@ CONFIGS = [
     ("N4 gated [1,4216,8192]", "gated", 1, 4216, 8192, False),
     ("N1 ln+fp8 [1,4216,4096]", "lnfp8", 1, 4216, 4096, False),
     ("N1 ln+fp8 [1,4096,3072]", "lnfp8", 1, 4096, 3072, False),
+    ("N2 gated ln [1,4216,4096]", "gatedln", 1, 4216, 4096, False),
+    ("N2 gated ln [1,4096,3072]", "gatedln", 1, 4096, 3072, False),
 ]
 
 
@@ -649,8 +651,8 @@ def config_bytes(kind, B, T, D, weight):
     """Algorithmic bytes and rows of one launch of a configuration."""
     if kind == "qk":
         return kernel_bytes()["qk_norm_rope_epilogue"]
-    rows, nvec = B * T, {"rms": 2, "ln": 2, "gated": 3, "lnfp8": 2}[kind]
-    io = {"rms": 4, "ln": 4, "gated": 8, "lnfp8": 3}[kind]  # bytes per element read + written
+    rows, nvec = B * T, {"rms": 2, "ln": 2, "gated": 3, "lnfp8": 2, "gatedln": 3}[kind]
+    io = {"rms": 4, "ln": 4, "gated": 8, "lnfp8": 3, "gatedln": 8}[kind]  # bytes per element
     return io * rows * D + nvec * B * D * 2 + (D * 2 if weight else 0), rows
 
 
@@ -684,7 +686,7 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
                 ydt = torch.uint8 if kind == "lnfp8" else torch.bfloat16
                 st = dict(x=rnd(B, T, D), emb=emb, y=torch.empty(B, T, D, dtype=ydt, device=dev),
                           w=(1.0 + rnd(D, std=0.05).float()).to(torch.bfloat16) if weight else None)
-                if kind == "gated":
+                if kind in ("gated", "gatedln"):
                     st.update(h=rnd(B, T, D), r_out=torch.empty(B, T, D, dtype=torch.bfloat16, device=dev))
                 sets.append(st)
         if kind == "qk":
@@ -706,6 +708,9 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
                 ops.ln_modulate(st["x"], vec(0), vec(1), EPS, out=st["y"])
             elif kind == "lnfp8":
                 ops.ln_modulate_fp8(st["x"], vec(0), vec(1), 0.05, EPS, out=st["y"])
+            elif kind == "gatedln":
+                ops.gated_ln_modulate(st["x"], st["h"], vec(0), vec(1), vec(2), EPS,
+                                      r_out=st["r_out"], out=st["y"])
             else:
                 ops.gated_rms_modulate(st["x"], st["h"], vec(0), vec(1), vec(2), EPS,
                                        r_out=st["r_out"], out=st["y"])

@@ -143,6 +143,22 @@ int validate_ln(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
     return check_buffers(ins, 3, outs, 1, inplace, 1);
 }
 
+int validate_gated_ln(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate,
+                      const dan_bf16 *scale, const dan_bf16 *shift, int64_t vs,
+                      const dan_bf16 *r_out, const dan_bf16 *y, int64_t B, int64_t T, int64_t D,
+                      float eps, bool *empty)
+{
+    int st = check_rows(B, T, D, eps, vs, ln_d_ok(D));
+    *empty = (st == DAN_OK && B * T == 0);
+    if (st != DAN_OK || *empty) return st;
+    const int64_t rows = B * T * D * 2, vb = vec_bytes(B, D, vs);
+    Buf ins[5] = {{r, span(r, rows)},     {h, span(h, rows)},       {gate, span(gate, vb)},
+                  {scale, span(scale, vb)}, {shift, span(shift, vb)}};
+    Buf outs[2] = {{r_out, span(r_out, rows)}, {y, span(y, rows)}};
+    const int inplace[1][2] = {{0, 0}}; // r_out == r
+    return check_buffers(ins, 5, outs, 2, inplace, 1);
+}
+
 int validate_ln_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift, int64_t vs,
                     float qscale, const uint8_t *q, int64_t B, int64_t T, int64_t D, float eps,
                     bool *empty)
@@ -371,6 +387,29 @@ int dan_ln_modulate(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *sh
     dan::RowProblem p{x, nullptr, nullptr, nullptr, scale, shift, vec_bstride, y, nullptr,
                       B, T, D, eps};
     return launched(dan::launch_ln_modulate(p, static_cast<cudaStream_t>(stream)));
+}
+
+int dan_can_use_gated_ln_modulate(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate,
+                                  const dan_bf16 *scale, const dan_bf16 *shift,
+                                  int64_t vec_bstride, const dan_bf16 *r_out, const dan_bf16 *y,
+                                  int64_t B, int64_t T, int64_t D, float eps)
+{
+    bool empty;
+    return validate_gated_ln(r, h, gate, scale, shift, vec_bstride, r_out, y, B, T, D, eps,
+                             &empty);
+}
+
+int dan_gated_ln_modulate(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate,
+                          const dan_bf16 *scale, const dan_bf16 *shift, int64_t vec_bstride,
+                          dan_bf16 *r_out, dan_bf16 *y, int64_t B, int64_t T, int64_t D,
+                          float eps, void *stream)
+{
+    bool empty;
+    const int st = validate_gated_ln(r, h, gate, scale, shift, vec_bstride, r_out, y, B, T, D,
+                                     eps, &empty);
+    if (st != DAN_OK || empty) return st;
+    dan::RowProblem p{r, h, gate, nullptr, scale, shift, vec_bstride, y, r_out, B, T, D, eps};
+    return launched(dan::launch_gated_ln_modulate(p, static_cast<cudaStream_t>(stream)));
 }
 
 int dan_can_use_ln_modulate_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,

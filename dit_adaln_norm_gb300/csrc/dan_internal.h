@@ -61,6 +61,7 @@ cudaError_t launch_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_gated_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_ln_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_ln_modulate_fp8(const RowProblem &p, cudaStream_t s);
+cudaError_t launch_gated_ln_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &p, cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).

@@ -473,12 +473,11 @@ __device__ __forceinline__ void ln_final(const Welford (&W)[4], float &mean, flo
 
 // Normalise, modulate and store (FP8: quantise and store) the logical warps
 // r + TW*m of a row.
-template <int FPT, int J, int TW, bool RAGGED, bool STAGED, bool FP8>
+template <int FPT, int J, int TW, bool RAGGED, bool STAGED, bool FP8, int NV>
 __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, float mean, float m2,
                                          const RowParams &p, int64_t row, int64_t bidx,
                                          const uint4 *s_vec, int lane)
 {
-    constexpr int NV = 2;
     const int F = p.F;
     const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
     const float2 mean2 = dup2(mean);
@@ -530,12 +529,13 @@ __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, flo
 
 // ------------------------------------------------------- the row kernel
 
-enum RowKind { kRms = 0, kGated = 1, kLn = 2, kLnFp8 = 3 };
+enum RowKind { kRms = 0, kGated = 1, kLn = 2, kLnFp8 = 3, kGatedLn = 4 };
 
 template <int KIND>
 struct RowShape {
-    static constexpr int NIN = KIND == kGated ? 2 : 1; // bulk-copied inputs per row
-    static constexpr int NV = KIND == kGated ? 3 : 2;  // staged vectors per batch
+    static constexpr bool GATED = KIND == kGated || KIND == kGatedLn;
+    static constexpr int NIN = GATED ? 2 : 1; // bulk-copied inputs per row
+    static constexpr int NV = GATED ? 3 : 2;  // staged vectors per batch
 };
 
 // Team exchange: per team and row parity, the logical warp results of a
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(32 * NW, 1)
     using Pipe = WarpPipe<SPC>;
     using Lay = RowLayout<KIND, NW, TW, SPC>;
     constexpr int NIN = Shape::NIN, NV = Shape::NV, NT = Lay::NT;
-    constexpr bool LN = KIND == kLn || KIND == kLnFp8;
+    constexpr bool LN = KIND == kLn || KIND == kLnFp8 || KIND == kGatedLn;
     constexpr int LWW = LN ? 1 : LW / TW; // RMS logical warps per warp
     constexpr int J = LN ? 4 / TW : 1;     // LayerNorm logical warps per warp
     static_assert(NW % TW == 0, "teams of TW warps");
@@ -681,7 +681,18 @@ __global__ void __launch_bounds__(32 * NW, 1)
 #pragma unroll
                 for (int q = 0; q < FPT; ++q) {
                     const int f = ln_frag(r + TW * m, lane, q);
-                    widen8((!RAGGED || f < F) ? src[f] : make_uint4(0, 0, 0, 0), x[m][q]);
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (!RAGGED || f < F) {
+                        v = src[f];
+                        if (KIND == kGatedLn) { // r' = bf16(r + bf16(gate * h)), stored at once
+                            const uint4 g = vec_frag<NV, STAGED>(p, s_vec, bidx, f, 2);
+                            const uint4 hh = src[F + f];
+                            v = make_uint4(gated_word(v.x, g.x, hh.x), gated_word(v.y, g.y, hh.y),
+                                           gated_word(v.z, g.z, hh.z), gated_word(v.w, g.w, hh.w));
+                            st_stream(p.r_out + row * F + f, v);
+                        }
+                    }
+                    widen8(v, x[m][q]);
                 }
             slot_reads_done();
             if (!refill()) {
@@ -713,8 +724,8 @@ __global__ void __launch_bounds__(32 * NW, 1)
                 for (int m = 0; m < 4; ++m) all[m] = Welford{xch[3 * m], xch[3 * m + 1], xch[3 * m + 2]};
             float mean, m2;
             ln_final<RAGGED>(all, mean, m2);
-            ln_store<FPT, J, TW, RAGGED, STAGED, KIND == kLnFp8>(x, r, mean, m2, p, row, bidx,
-                                                                 s_vec, lane);
+            ln_store<FPT, J, TW, RAGGED, STAGED, KIND == kLnFp8, NV>(x, r, mean, m2, p, row, bidx,
+                                                                     s_vec, lane);
         } else {
             float x[LWW][8][8];
             const int j0 = r * LWW;

@@ -34,6 +34,8 @@ _SIGS = {
     "dan_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F, _P],
     "dan_can_use_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F],
     "dan_ln_modulate_fp8": [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F, _P],
+    "dan_gated_ln_modulate": [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F, _P],
+    "dan_can_use_gated_ln_modulate": [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F],
     "dan_can_use_ln_modulate_fp8": [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F],
     "dan_qk_norm_rope_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
                                   _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P],
@@ -185,6 +187,21 @@ def ln_modulate(x, scale, shift, eps: float, out=None):
     _check(load().dan_ln_modulate(_ptr(x), _ptr(scale), _ptr(shift), vs, _ptr(y), B, T, D,
                                   float(eps), _stream()), "dan_ln_modulate")
     return y
+
+
+def gated_ln_modulate(r, h, gate, scale, shift, eps: float, r_out=None, out=None):
+    """r' = bf16(r + bf16(gate * h)); y = ln_modulate(r').  Returns (r', y)."""
+    B, T, D = _rows(r, "r")
+    _rows(h, "h")
+    vs = _vectors(B, D, [("gate", gate), ("scale", scale), ("shift", shift)])
+    r_out = torch.empty_like(r) if r_out is None else r_out
+    y = torch.empty_like(r) if out is None else out
+    _rows(r_out, "r_out")
+    _rows(y, "out")
+    _check(load().dan_gated_ln_modulate(_ptr(r), _ptr(h), _ptr(gate), _ptr(scale), _ptr(shift),
+                                        vs, _ptr(r_out), _ptr(y), B, T, D, float(eps),
+                                        _stream()), "dan_gated_ln_modulate")
+    return r_out, y
 
 
 def ln_modulate_fp8(x, scale, shift, qscale: float, eps: float, out=None):

@@ -1,10 +1,11 @@
 /*
  * dan.h -- C ABI of the GB300 (sm_103a) fused adaLN norm+modulate kernels.
  *
- * Five operations, each a single kernel launch on the caller's stream:
+ * Six operations, each a single kernel launch on the caller's stream:
  *
  *   dan_ln_modulate         y = bf16(LayerNorm(x) * (1 + scale) + shift)
  *   dan_ln_modulate_fp8     q = e4m3(y * rn(1/qscale)), y as dan_ln_modulate
+ *   dan_gated_ln_modulate   r' = bf16(r + bf16(gate * h)); y = ln_modulate(r')
  *   dan_rms_modulate        y = bf16(RMSNorm(x) [* w] * (1 + scale) + shift)
  *   dan_gated_rms_modulate  r' = bf16(r + bf16(gate * h)); y = rms_modulate(r')
  *   dan_qk_norm_rope_epilogue  per-head RMSNorm + interleaved RoPE of Q and K,
@@ -172,6 +173,23 @@ int dan_ln_modulate(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *sh
 int dan_can_use_ln_modulate(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,
                             int64_t vec_bstride, const dan_bf16 *y, int64_t B, int64_t T,
                             int64_t D, float eps);
+
+/* ------------------------------------------------------ gated LayerNorm
+ * The residual variant of the guide's "Norm + scale/shift (adaLN)" section
+ * (round(gate * update), then round(residual + that), the rounded result
+ * fed to the same norm) with the LayerNorm above:
+ *   r_out = bf16(rn(r + bf16(rn(gate * h)))),  y = dan_ln_modulate(r_out)
+ * bit for bit.  gate, scale, shift share vec_bstride.  Supported D as for
+ * dan_ln_modulate.  In place: r_out == r is allowed; y may not overlap
+ * r_out or any input. */
+int dan_gated_ln_modulate(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate,
+                          const dan_bf16 *scale, const dan_bf16 *shift, int64_t vec_bstride,
+                          dan_bf16 *r_out, dan_bf16 *y, int64_t B, int64_t T, int64_t D,
+                          float eps, void *stream);
+int dan_can_use_gated_ln_modulate(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate,
+                                  const dan_bf16 *scale, const dan_bf16 *shift,
+                                  int64_t vec_bstride, const dan_bf16 *r_out, const dan_bf16 *y,
+                                  int64_t B, int64_t T, int64_t D, float eps);
 
 /* ------------------------------------------- LayerNorm + modulate + FP8
  * "SGLang diffusion fused-op package guide", list of fused producers:

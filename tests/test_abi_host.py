@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = ops.declared_symbols()
-    assert len(names) == 14
+    assert len(names) == 16
     for n in names:
         assert hasattr(lib, n), n
 
@@ -90,6 +90,16 @@ def test_ln_validation(lib):
         assert f(D=D, vs=max(D, 8)) == EUNSUP, D
     assert f(y=X) == OK and f(y=X + 16) == EALIAS
     assert f(B=2, vs=6 * 3072) == OK and f(B=2, vs=3076) == EALIGN
+
+
+def test_gated_ln_validation(lib):
+    def f(r=R, h=H, g=G, sc=SC, sh=SH, vs=3072, ro=RO, y=Y, B=1, T=4096, D=3072, eps=EPS):
+        return lib.dan_can_use_gated_ln_modulate(r, h, g, sc, sh, vs, ro, y, B, T, D, eps)
+
+    assert f() == OK and f(D=1040, vs=1040) == OK
+    assert f(ro=R) == OK               # residual updated in place
+    assert f(y=R) == EALIAS and f(ro=H) == EALIAS and f(y=RO) == EALIAS
+    assert f(D=12, vs=16) == EUNSUP and f(g=None) == EINVAL and f(h=G + 8) == EALIGN
 
 
 def test_ln_fp8_validation(lib):

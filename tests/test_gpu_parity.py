@@ -355,3 +355,36 @@ def test_ln_fp8_extreme_rows():
 def test_ln_fp8_metric_shape_and_cfg_batch():
     run_ln_fp8(1, 4216, 4096, synth.SEED_X, 0.05)
     run_ln_fp8(2, 1140, 4096, synth.SEED_X + 1, 0.05)
+
+
+# ------------------------------------------------ gated residual + LayerNorm
+
+def run_gated_ln(B, T, D, seed, inplace=False, chunks=6):
+    r = synth.outlier_rows_bf16((B, T, D), seed, synth.SEED_OUTLIER)
+    h = synth.normal_bf16((B, T, D), seed + 1)
+    (g, sc, sh), (dg, dsc, dsh) = adaln(B, D, 3, seed + 2, 0.1, chunks)
+    dr = to_dev(r)
+    buf, y = guarded((B, T, D))
+    if inplace:
+        r_out = dr
+    else:
+        rbuf, r_out = guarded((B, T, D))
+    ops.gated_ln_modulate(dr, to_dev(h), dg, dsc, dsh, EPS, r_out=r_out, out=y)
+    torch.cuda.synchronize()
+    check_guard(buf)
+    if not inplace:
+        check_guard(rbuf)
+    want_r, want_y = oracle.gated_ln_modulate(r, h, g, sc, sh, EPS)
+    assert_bits_equal(from_dev(r_out), want_r, f"gated ln r' D={D}")
+    assert_bits_equal(from_dev(y), want_y, f"gated ln y D={D}")
+
+
+@pytest.mark.parametrize("D", [8, 1040, 3072, 4096, 5000, 8192])
+def test_gated_ln_small(D):
+    run_gated_ln(2, 23, D, 500 + D)
+
+
+def test_gated_ln_in_place_and_shapes():
+    run_gated_ln(1, 97, 3072, 510, inplace=True)
+    run_gated_ln(1, 4216, 4096, synth.SEED_X)
+    run_gated_ln(2, 1140, 4096, synth.SEED_X + 2)
