@@ -18,7 +18,9 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   parenthesisation and the cross-warp order are this library's definition:
   they are fixed by the tests only through the GPU == oracle comparison.
 * ``qk_norm_rope_epilogue``: pinned (cos=1/sin=0 and cos=0/sin=1 rotations,
-  V copy, joint order, fp64 brute force).
+  V copy, joint order, fp64 brute force); with head_dim 64 and the neox
+  rotation: the same closed forms, the neox rotation as a column
+  permutation of the interleaved one, fp64 brute force.
 * ``gated_ln_modulate``: pinned (r' against an independent elementwise
   formula, gate = 0 and the composition with ``ln_modulate`` of r').
 * ``fp8_e4m3``: pinned (every finite code decodes and re-encodes to itself,
@@ -74,6 +76,9 @@ def _load():
         lib.oracle_qk_norm_rope_epilogue.argtypes = (
             [_P, _P, _P, _I, _I] + [_P, _P, _P, _I, _I] + [_I] + [_P] * 4 + [_P, _P]
             + [_F, _F] + [_P, _P, _P, _P])
+        lib.oracle_qk_norm_rope.argtypes = (
+            [_P, _P, _P, _I, _I] + [_P, _P, _P, _I, _I] + [_I, ctypes.c_int, ctypes.c_int]
+            + [_P] * 4 + [_P, _P] + [_F, _F] + [_P, _P, _P, _P])
         for f in ("oracle_round_bf16", "oracle_rms_modulate", "oracle_gated_rms_modulate",
                   "oracle_ln_modulate", "oracle_qk_norm_rope_epilogue"):
             getattr(lib, f).restype = None
@@ -176,14 +181,14 @@ def ln_modulate(x, scale, shift, eps, with_stats=False):
 
 
 def _qkv_views(q, k, v, name):
-    """q, k, v: [T, H*128] views sharing one row stride (unit column stride)."""
+    """q, k, v: [T, H*head_dim] views sharing one row stride (unit column stride)."""
     arrs = [_bits(a, f"{name}.{n}") for a, n in zip((q, k, v), "qkv")]
     T, HD = arrs[0].shape
     if T == 0:  # an empty stream: nothing is read, strides are irrelevant
         return [np.zeros((0, HD), np.uint16)] * 3, 0, HD, HD
     for a in arrs:
         if a.shape != (T, HD) or a.strides[1] != 2:
-            raise ValueError(f"{name}: q, k, v must be [T, H*128] views, unit column stride")
+            raise ValueError(f"{name}: q, k, v must be [T, H*head_dim] views, unit column stride")
     strides = {a.strides[0] // 2 for a in arrs}
     if len(strides) != 1:
         raise ValueError(f"{name}: q, k, v must share one row stride")
@@ -191,28 +196,32 @@ def _qkv_views(q, k, v, name):
 
 
 def qk_norm_rope_epilogue(txt, img, H, weights, rope_txt, rope_img, eps_txt, eps_img,
-                          with_stats=False):
-    """txt, img: (q, k, v) views [T_s, H*128]; weights: (wq_txt, wk_txt, wq_img,
-    wk_img) [128] bf16; rope_*: fp32 [T_s, 128].  Returns joint q, k, v as
-    [T_txt + T_img, H, 128] (and rstd [T, 2, H] if with_stats)."""
+                          with_stats=False, head_dim=128, neox=False):
+    """txt, img: (q, k, v) views [T_s, H*head_dim]; weights: (wq_txt, wk_txt,
+    wq_img, wk_img) [head_dim] bf16; rope_*: fp32 [T_s, head_dim].  Returns
+    joint q, k, v as [T_txt + T_img, H, head_dim] (and rstd [T, 2, H] if
+    with_stats).  head_dim 128 or 64; neox rotates (i, i + head_dim/2)
+    instead of interleaved pairs."""
+    if head_dim not in (64, 128):
+        raise ValueError("head_dim must be 64 or 128")
     (qt, kt, vt), Tt, HDt, st_ = _qkv_views(*txt, "txt")
     (qi, ki, vi), Ti, HDi, si_ = _qkv_views(*img, "img")
-    if HDt != H * 128 or HDi != H * 128:
-        raise ValueError("head_dim must be 128")
+    if HDt != H * head_dim or HDi != H * head_dim:
+        raise ValueError("q, k, v must be [T, H*head_dim]")
     ws = [np.ascontiguousarray(_bits(w, "weight")) for w in weights]
     rt = np.ascontiguousarray(rope_txt, dtype=np.float32)
     ri = np.ascontiguousarray(rope_img, dtype=np.float32)
-    if rt.shape != (Tt, 128) or ri.shape != (Ti, 128):
-        raise ValueError("rope tables must be [T_s, 128] fp32")
+    if rt.shape != (Tt, head_dim) or ri.shape != (Ti, head_dim):
+        raise ValueError("rope tables must be [T_s, head_dim] fp32")
     T = Tt + Ti
-    qo = np.empty((T, H, 128), np.uint16)
+    qo = np.empty((T, H, head_dim), np.uint16)
     ko = np.empty_like(qo)
     vo = np.empty_like(qo)
     rs = np.empty((T, 2, H), np.float32) if with_stats else None
-    _load().oracle_qk_norm_rope_epilogue(
+    _load().oracle_qk_norm_rope(
         _ptr(qt), _ptr(kt), _ptr(vt), Tt, st_, _ptr(qi), _ptr(ki), _ptr(vi), Ti, si_, H,
-        *[_ptr(w) for w in ws], _ptr(rt), _ptr(ri), float(eps_txt), float(eps_img),
-        _ptr(qo), _ptr(ko), _ptr(vo), _ptr(rs))
+        head_dim, int(bool(neox)), *[_ptr(w) for w in ws], _ptr(rt), _ptr(ri), float(eps_txt),
+        float(eps_img), _ptr(qo), _ptr(ko), _ptr(vo), _ptr(rs))
     return (qo, ko, vo, rs) if with_stats else (qo, ko, vo)
 
 

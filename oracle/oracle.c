@@ -320,68 +320,92 @@ void oracle_gated_ln_modulate(const bf16_bits *r, const bf16_bits *h, const bf16
 
 /* ------------------------------------------------- QK norm + RoPE + V */
 
-/* RMS of one head of 128 values: 16 logical threads, thread l owns columns
- * 8l..8l+7 as one chain; the 16 partials fold by the adjacent-pair tree. */
-static float head_rstd(const float *x, float eps)
+/* RMS of one head of hd values (hd = 128 or 64): hd/8 logical threads,
+ * thread l owns columns 8l..8l+7 as one chain; the partials fold by the
+ * adjacent-pair tree. */
+static float head_rstd(const float *x, int hd, float eps)
 {
     float lane[16];
-    for (int l = 0; l < 16; ++l) {
+    const int L = hd / 8;
+    for (int l = 0; l < L; ++l) {
         float acc = 0.0f;
         for (int v = 0; v < 8; ++v)
             acc = rn_add(acc, rn_mul(x[8 * l + v], x[8 * l + v]));
         lane[l] = acc;
     }
-    for (int off = 1; off < 16; off *= 2)
-        for (int i = 0; i < 16; i += 2 * off)
+    for (int off = 1; off < L; off *= 2)
+        for (int i = 0; i < L; i += 2 * off)
             lane[i] = rn_add(lane[i], lane[i + off]);
-    return defined_rsqrt(rn_add(rn_div(lane[0], 128.0f), eps));
+    return defined_rsqrt(rn_add(rn_div(lane[0], (float)hd), eps));
 }
 
-/* Normalise one head with weight w, then rotate pairs (2i, 2i+1) by the
- * cos/sin of cache row rope ([cos_0..cos_63 | sin_0..sin_63], fp32). */
-static float qk_head(const bf16_bits *src, const bf16_bits *w, const float *rope,
-                     float eps, bf16_bits *dst)
+/* Normalise one head with weight w, then rotate by the cos/sin of cache row
+ * rope ([cos_0..cos_{hd/2-1} | sin_0..sin_{hd/2-1}], fp32): interleaved
+ * pairs (2i, 2i+1), or with neox != 0 the halves' pairs (i, i + hd/2). */
+static float qk_head(const bf16_bits *src, const bf16_bits *w, const float *rope, int hd,
+                     int neox, float eps, bf16_bits *dst)
 {
     float x[128], n[128];
-    for (int j = 0; j < 128; ++j)
+    const int half = hd / 2;
+    for (int j = 0; j < hd; ++j)
         x[j] = widen(src[j]);
-    float rstd = head_rstd(x, eps);
-    for (int j = 0; j < 128; ++j)
+    float rstd = head_rstd(x, hd, eps);
+    for (int j = 0; j < hd; ++j)
         n[j] = bf(rn_mul(rn_mul(x[j], rstd), widen(w[j])));
-    for (int i = 0; i < 64; ++i) {
-        float c = rope[i], s = rope[64 + i];
-        float a = n[2 * i], b = n[2 * i + 1];
-        dst[2 * i] = narrow(rn_sub(rn_mul(a, c), rn_mul(b, s)));
-        dst[2 * i + 1] = narrow(rn_add(rn_mul(a, s), rn_mul(b, c)));
+    for (int i = 0; i < half; ++i) {
+        const float c = rope[i], s = rope[half + i];
+        const int ia = neox ? i : 2 * i, ib = neox ? i + half : 2 * i + 1;
+        const float a = n[ia], b = n[ib];
+        dst[ia] = narrow(rn_sub(rn_mul(a, c), rn_mul(b, s)));
+        dst[ib] = narrow(rn_add(rn_mul(a, s), rn_mul(b, c)));
     }
     return rstd;
 }
 
 static void qk_stream(const bf16_bits *q, const bf16_bits *k, const bf16_bits *v, int64_t T,
-                      int64_t stride, int64_t H, const bf16_bits *wq, const bf16_bits *wk,
-                      const float *rope, float eps, int64_t out_row0, bf16_bits *q_out,
-                      bf16_bits *k_out, bf16_bits *v_out, float *rstd_out)
+                      int64_t stride, int64_t H, int hd, int neox, const bf16_bits *wq,
+                      const bf16_bits *wk, const float *rope, float eps, int64_t out_row0,
+                      bf16_bits *q_out, bf16_bits *k_out, bf16_bits *v_out, float *rstd_out)
 {
     for (int64_t t = 0; t < T; ++t) {
         int64_t orow = out_row0 + t;
-        for (int64_t hd = 0; hd < H; ++hd) {
-            int64_t src = t * stride + hd * 128;
-            int64_t dst = (orow * H + hd) * 128;
-            float rq = qk_head(q + src, wq, rope + t * 128, eps, q_out + dst);
-            float rk = qk_head(k + src, wk, rope + t * 128, eps, k_out + dst);
-            memcpy(v_out + dst, v + src, 128 * sizeof(bf16_bits));
+        for (int64_t h = 0; h < H; ++h) {
+            int64_t src = t * stride + h * hd;
+            int64_t dst = (orow * H + h) * hd;
+            float rq = qk_head(q + src, wq, rope + t * hd, hd, neox, eps, q_out + dst);
+            float rk = qk_head(k + src, wk, rope + t * hd, hd, neox, eps, k_out + dst);
+            memcpy(v_out + dst, v + src, (size_t)hd * sizeof(bf16_bits));
             if (rstd_out) {
-                rstd_out[(orow * 2 + 0) * H + hd] = rq;
-                rstd_out[(orow * 2 + 1) * H + hd] = rk;
+                rstd_out[(orow * 2 + 0) * H + h] = rq;
+                rstd_out[(orow * 2 + 1) * H + h] = rk;
             }
         }
     }
 }
 
-/* Q/K: per-head RMSNorm with weight then interleaved RoPE; V: copy.  Inputs
- * are row-strided views (row stride in elements, heads contiguous at 128);
- * outputs are [T_txt + T_img, H, 128], text rows first.  rstd_out
+/* Q/K: per-head RMSNorm with weight then RoPE; V: copy.  Inputs are
+ * row-strided views (row stride in elements, heads contiguous at hd);
+ * outputs are [T_txt + T_img, H, hd], text rows first.  hd is 128 or 64;
+ * neox selects the rotation of halves instead of interleaved pairs (the
+ * interleaved form is the Qwen epilogue's is_neox=False).  rstd_out
  * (nullable): [T_txt + T_img, 2 (q,k), H]. */
+void oracle_qk_norm_rope(const bf16_bits *q_txt, const bf16_bits *k_txt, const bf16_bits *v_txt,
+                         int64_t T_txt, int64_t txt_stride, const bf16_bits *q_img,
+                         const bf16_bits *k_img, const bf16_bits *v_img, int64_t T_img,
+                         int64_t img_stride, int64_t H, int hd, int neox,
+                         const bf16_bits *wq_txt, const bf16_bits *wk_txt,
+                         const bf16_bits *wq_img, const bf16_bits *wk_img,
+                         const float *rope_txt, const float *rope_img, float eps_txt,
+                         float eps_img, bf16_bits *q_out, bf16_bits *k_out, bf16_bits *v_out,
+                         float *rstd_out)
+{
+    qk_stream(q_txt, k_txt, v_txt, T_txt, txt_stride, H, hd, neox, wq_txt, wk_txt, rope_txt,
+              eps_txt, 0, q_out, k_out, v_out, rstd_out);
+    qk_stream(q_img, k_img, v_img, T_img, img_stride, H, hd, neox, wq_img, wk_img, rope_img,
+              eps_img, T_txt, q_out, k_out, v_out, rstd_out);
+}
+
+/* The Qwen epilogue: head_dim 128, interleaved pairs. */
 void oracle_qk_norm_rope_epilogue(const bf16_bits *q_txt, const bf16_bits *k_txt,
                                   const bf16_bits *v_txt, int64_t T_txt, int64_t txt_stride,
                                   const bf16_bits *q_img, const bf16_bits *k_img,
@@ -392,10 +416,9 @@ void oracle_qk_norm_rope_epilogue(const bf16_bits *q_txt, const bf16_bits *k_txt
                                   float eps_img, bf16_bits *q_out, bf16_bits *k_out,
                                   bf16_bits *v_out, float *rstd_out)
 {
-    qk_stream(q_txt, k_txt, v_txt, T_txt, txt_stride, H, wq_txt, wk_txt, rope_txt, eps_txt, 0,
-              q_out, k_out, v_out, rstd_out);
-    qk_stream(q_img, k_img, v_img, T_img, img_stride, H, wq_img, wk_img, rope_img, eps_img,
-              T_txt, q_out, k_out, v_out, rstd_out);
+    oracle_qk_norm_rope(q_txt, k_txt, v_txt, T_txt, txt_stride, q_img, k_img, v_img, T_img,
+                        img_stride, H, 128, 0, wq_txt, wk_txt, wq_img, wk_img, rope_txt,
+                        rope_img, eps_txt, eps_img, q_out, k_out, v_out, rstd_out);
 }
 
 /* ------------------------------------------- LayerNorm + modulate + FP8 */

@@ -620,3 +620,75 @@ def test_gated_ln_zero_gate_is_ln_of_residual(orc):
     r_out, y = orc.gated_ln_modulate(r, h, zeros, scale, shift, EPS)
     assert np.array_equal(r_out, r)
     assert np.array_equal(y, orc.ln_modulate(r, scale, shift, EPS))
+
+
+# ------------------------------- QK epilogue: head_dim 64 and neox rotation
+
+def _rope_const_hd(T, hd, c, s):
+    return np.concatenate([np.full((T, hd // 2), c, np.float32),
+                           np.full((T, hd // 2), s, np.float32)], 1)
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_qk_neox_identity_and_quarter_turn(orc, hd):
+    """neox: cos = 1, sin = 0 leaves the normalised head as the interleaved
+    identity does; cos = 0, sin = 1 maps (x_i, x_{i+h}) to (-x_{i+h}, x_i)."""
+    Tt, Ti, H = 3, 4, 3
+    pt, pi = synth.packed_qkv(Tt, H, 70, hd), synth.packed_qkv(Ti, H, 71, hd)
+    ws = synth.head_weights(4, 72, hd)
+    txt, img = synth.split_qkv(pt, H, hd), synth.split_qkv(pi, H, hd)
+    run = lambda c, s, neox: orc.qk_norm_rope_epilogue(
+        txt, img, H, ws, _rope_const_hd(Tt, hd, c, s), _rope_const_hd(Ti, hd, c, s), EPS, EPS,
+        head_dim=hd, neox=neox)
+    q_id, k_id, _ = run(1, 0, False)
+    q1, k1, v1 = run(1, 0, True)
+    q2, k2, v2 = run(0, 1, True)
+    assert np.array_equal(q1, q_id) and np.array_equal(k1, k_id)
+    h = hd // 2
+    for n, r in ((q1, q2), (k1, k2)):
+        nf, rf = widen(n), widen(r)
+        assert np.array_equal(rf[..., :h], -nf[..., h:])
+        assert np.array_equal(rf[..., h:], nf[..., :h])
+    assert np.array_equal(v1, v2) and np.array_equal(v1.reshape(Tt + Ti, -1)[:Tt], txt[2])
+
+
+def test_qk_head_dim_64_unit_head(orc):
+    Tt, Ti, H, hd = 2, 3, 5, 64
+    sgn = np.where(np.random.Generator(np.random.PCG64(73)).random((Tt + Ti, 3 * H * hd)) < 0.5,
+                   -1.0, 1.0)
+    packed = bits_of(sgn)
+    ones = [bits_of(np.ones(hd))] * 4
+    q, k, _ = orc.qk_norm_rope_epilogue(synth.split_qkv(packed[:Tt], H, hd),
+                                        synth.split_qkv(packed[Tt:], H, hd), H, ones,
+                                        _rope_const_hd(Tt, hd, 1, 0),
+                                        _rope_const_hd(Ti, hd, 1, 0), EPS, EPS, head_dim=hd)
+    W = H * hd
+    assert np.array_equal(widen(q).reshape(-1, W), sgn[:, :W].astype(np.float32))
+    assert np.array_equal(widen(k).reshape(-1, W), sgn[:, W:2 * W].astype(np.float32))
+
+
+@pytest.mark.parametrize("hd,neox", [(64, False), (64, True), (128, True)])
+def test_qk_variants_fp64_brute_force(orc, hd, neox):
+    Tt, Ti, H = 6, 20, 3
+    pt, pi = synth.packed_qkv(Tt, H, 74, hd), synth.packed_qkv(Ti, H, 75, hd)
+    ws = synth.head_weights(4, 76, hd)
+    txt, img = synth.split_qkv(pt, H, hd), synth.split_qkv(pi, H, hd)
+    rt, ri = synth.rope_table(Tt, hd), synth.rope_table(Ti, hd, pos0=11)
+    q, k, _, rs = orc.qk_norm_rope_epilogue(txt, img, H, ws, rt, ri, EPS, EPS, with_stats=True,
+                                            head_dim=hd, neox=neox)
+    h = hd // 2
+    for src, rope, wq, wk, row0 in ((txt, rt, ws[0], ws[1], 0), (img, ri, ws[2], ws[3], Tt)):
+        T = src[0].shape[0]
+        for which, (x, w, out) in enumerate(((src[0], wq, q), (src[1], wk, k))):
+            xf = widen(x).astype(np.float64).reshape(T, H, hd)
+            rstd64 = 1.0 / np.sqrt((xf ** 2).mean(-1) + EPS)
+            assert np.all(np.abs(rs[row0:row0 + T, which, :] / rstd64 - 1.0) <= 1e-6)
+            n = bf16_of_f64(xf * rstd64[..., None] * widen(w).astype(np.float64))
+            a, b = (n[..., :h], n[..., h:]) if neox else (n[..., 0::2], n[..., 1::2])
+            c = rope[:, None, :h].astype(np.float64)
+            sn = rope[:, None, h:].astype(np.float64)
+            e0, e1 = a * c - b * sn, a * sn + b * c
+            tol = 2 * bf16_ulp(np.maximum(np.abs(a), np.abs(b)))
+            o = widen(out[row0:row0 + T]).astype(np.float64)
+            o0, o1 = (o[..., :h], o[..., h:]) if neox else (o[..., 0::2], o[..., 1::2])
+            assert np.all(np.abs(o0 - e0) <= tol) and np.all(np.abs(o1 - e1) <= tol)
