@@ -624,8 +624,11 @@ def run_ours(args, rank, world, dist):
 
 # The kernel configurations of the path: the metric's shapes and the
 # pages' other sites (FLUX.1 LayerNorm sites at D = 3072, the CFG batch of
-# two, the ERNIE RMS with weight at the larger hidden sizes).  Each is timed
-# alone; these are per-kernel figures, not part of the step.
+# two, the ERNIE RMS with weight at the larger hidden sizes), and the
+# variants built beyond them (LayerNorm + FP8, gated LayerNorm, QK with the
+# neox rotation and head_dim 64).  Each is timed alone; these are
+# per-kernel figures, not part of the step.  (name, kind, B, T, D, flag):
+# flag is the RMS weight, or for "qk" the neox rotation with D = head_dim.
 CONFIGS = [
     ("C1 rms [1,128,2048]", "rms", 1, 128, 2048, False),
     ("C1' rms [1,4216,4096]", "rms", 1, 4216, 4096, False),
@@ -636,7 +639,7 @@ CONFIGS = [
     ("C2' ln [1,4216,4096]", "ln", 1, 4216, 4096, False),
     ("C3 gated [1,4216,4096]", "gated", 1, 4216, 4096, False),
     ("C4 ln CFG [2,1140,4096]", "ln", 2, 1140, 4096, False),
-    ("C5 qk 256+4096 tokens x 24 heads x 128", "qk", 1, 0, 0, False),
+    ("C5 qk 256+4096 tokens x 24 heads x 128", "qk", 1, 0, 128, False),
     ("N4 rms+weight [1,4216,6144]", "rms", 1, 4216, 6144, True),
     ("N4 rms+weight [1,4216,8192]", "rms", 1, 4216, 8192, True),
     ("N4 gated [1,4216,8192]", "gated", 1, 4216, 8192, False),
@@ -644,13 +647,17 @@ CONFIGS = [
     ("N1 ln+fp8 [1,4096,3072]", "lnfp8", 1, 4096, 3072, False),
     ("N2 gated ln [1,4216,4096]", "gatedln", 1, 4216, 4096, False),
     ("N2 gated ln [1,4096,3072]", "gatedln", 1, 4096, 3072, False),
+    ("N3 qk neox 256+4096 tokens x 24 heads x 128", "qk", 1, 0, 128, True),
+    ("N3 qk 256+4096 tokens x 48 heads x 64", "qk", 1, 0, 64, False),
+    ("N3 qk neox 256+4096 tokens x 48 heads x 64", "qk", 1, 0, 64, True),
 ]
 
 
 def config_bytes(kind, B, T, D, weight):
     """Algorithmic bytes and rows of one launch of a configuration."""
-    if kind == "qk":
-        return kernel_bytes()["qk_norm_rope_epilogue"]
+    if kind == "qk":  # D is head_dim; 24 heads of 128 or 48 of 64
+        heads, tok = 24 * 128 // D, T_TXT + T_IMG
+        return 2 * tok * 3 * heads * D * 2 + 4 * D * 2 + tok * D * 4, tok
     rows, nvec = B * T, {"rms": 2, "ln": 2, "gated": 3, "lnfp8": 2, "gatedln": 3}[kind]
     io = {"rms": 4, "ln": 4, "gated": 8, "lnfp8": 3, "gatedln": 8}[kind]  # bytes per element
     return io * rows * D + nvec * B * D * 2 + (D * 2 if weight else 0), rows
@@ -675,10 +682,11 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
         sets = []
         for _ in range(nsets):
             if kind == "qk":
-                txt, img = rnd(T_TXT, 3 * HEADS * 128), rnd(T_IMG, 3 * HEADS * 128)
-                w = (1.0 + rnd(4, 128, std=0.05).float()).to(torch.bfloat16)
+                hd, heads = D, 24 * 128 // D
+                txt, img = rnd(T_TXT, 3 * heads * hd), rnd(T_IMG, 3 * heads * hd)
+                w = (1.0 + rnd(4, hd, std=0.05).float()).to(torch.bfloat16)
                 sets.append(dict(txt=txt, img=img, w=w,
-                                 out=tuple(torch.empty((T_TXT + T_IMG, HEADS, 128),
+                                 out=tuple(torch.empty((T_TXT + T_IMG, heads, hd),
                                                        dtype=torch.bfloat16, device=dev)
                                            for _ in range(3))))
             else:
@@ -691,15 +699,17 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
                 sets.append(st)
         if kind == "qk":
             from dit_adaln_norm_gb300 import synth
-            rope_t = torch.from_numpy(synth.rope_table(T_TXT)).to(dev)
-            rope_i = torch.from_numpy(synth.rope_table(T_IMG, pos0=T_TXT)).to(dev)
+            rope_t = torch.from_numpy(synth.rope_table(T_TXT, D)).to(dev)
+            rope_i = torch.from_numpy(synth.rope_table(T_IMG, D, pos0=T_TXT)).to(dev)
 
         def launch(st):
             if kind == "qk":
-                w = st["w"]
-                ops.qk_norm_rope_epilogue(split_qkv(st["txt"], HEADS), split_qkv(st["img"], HEADS),
-                                          w[0], w[1], w[2], w[3], rope_t, rope_i, EPS, EPS, HEADS,
-                                          out=st["out"])
+                w, hd = st["w"], D
+                heads = 24 * 128 // hd
+                ops.qk_norm_rope_epilogue(split_qkv(st["txt"], heads, hd),
+                                          split_qkv(st["img"], heads, hd), w[0], w[1], w[2], w[3],
+                                          rope_t, rope_i, EPS, EPS, heads, out=st["out"],
+                                          head_dim=hd, neox=weight)
                 return
             vec = lambda i: st["emb"][:, i * D:(i + 1) * D]
             if kind == "rms":

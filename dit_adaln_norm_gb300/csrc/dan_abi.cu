@@ -179,10 +179,10 @@ int validate_qk(const dan_bf16 *const qkv[2][3], const int64_t Ts[2], const int6
                 bool *empty)
 {
     if (Ts[0] < 0 || Ts[1] < 0 || heads < 0 || head_dim < 0) return DAN_EINVAL;
-    if (head_dim != 128) return DAN_EUNSUPPORTED;
+    if (head_dim != 128 && head_dim != 64) return DAN_EUNSUPPORTED;
     if (heads < 1 || heads > (int64_t(1) << 20)) return DAN_EINVAL;
     if (!eps_ok(eps[0]) || !eps_ok(eps[1])) return DAN_EINVAL;
-    const int64_t width = heads * 128;
+    const int64_t width = heads * head_dim;
     for (int s = 0; s < 2; ++s) {
         if (Ts[s] > kMaxElems / width) return DAN_EINVAL;
         if (Ts[s] > 0) {
@@ -201,9 +201,9 @@ int validate_qk(const dan_bf16 *const qkv[2][3], const int64_t Ts[2], const int6
         if (Ts[s] == 0) continue;
         const int64_t bytes = ((Ts[s] - 1) * strides[s] + width) * 2;
         for (int k = 0; k < 3; ++k) ins[nin++] = {qkv[s][k], span(qkv[s][k], bytes)};
-        ins[nin++] = {w[2 * s], span(w[2 * s], 256)};
-        ins[nin++] = {w[2 * s + 1], span(w[2 * s + 1], 256)};
-        ins[nin++] = {rope[s], span(rope[s], Ts[s] * 128 * 4)};
+        ins[nin++] = {w[2 * s], span(w[2 * s], head_dim * 2)};
+        ins[nin++] = {w[2 * s + 1], span(w[2 * s + 1], head_dim * 2)};
+        ins[nin++] = {rope[s], span(rope[s], Ts[s] * head_dim * 4)};
     }
     Buf outs[3];
     for (int k = 0; k < 3; ++k) outs[k] = {outs_p[k], span(outs_p[k], T * width * 2)};
@@ -211,6 +211,50 @@ int validate_qk(const dan_bf16 *const qkv[2][3], const int64_t Ts[2], const int6
 }
 
 int launched(cudaError_t e) { return e == cudaSuccess ? DAN_OK : DAN_ECUDA; }
+
+// The QK epilogue's arguments as the C entry points take them.
+struct QkArgs {
+    const dan_bf16 *q_txt, *k_txt, *v_txt;
+    int64_t T_txt, txt_row_stride;
+    const dan_bf16 *q_img, *k_img, *v_img;
+    int64_t T_img, img_row_stride, heads, head_dim;
+    const dan_bf16 *wq_txt, *wk_txt, *wq_img, *wk_img;
+    const float *rope_txt, *rope_img;
+    float eps_txt, eps_img;
+    const dan_bf16 *q_out, *k_out, *v_out;
+};
+
+// Validate, and unless `check_only` launch, one QK epilogue call.
+int qk_call(const QkArgs &a, bool neox, bool check_only, void *stream)
+{
+    const dan_bf16 *const qkv[2][3] = {{a.q_txt, a.k_txt, a.v_txt}, {a.q_img, a.k_img, a.v_img}};
+    const int64_t Ts[2] = {a.T_txt, a.T_img}, strides[2] = {a.txt_row_stride, a.img_row_stride};
+    const dan_bf16 *const w[4] = {a.wq_txt, a.wk_txt, a.wq_img, a.wk_img};
+    const float *const rope[2] = {a.rope_txt, a.rope_img};
+    const float eps[2] = {a.eps_txt, a.eps_img};
+    const dan_bf16 *const outs[3] = {a.q_out, a.k_out, a.v_out};
+    bool empty;
+    const int st = validate_qk(qkv, Ts, strides, a.heads, a.head_dim, w, rope, eps, outs, &empty);
+    if (st != DAN_OK || empty || check_only) return st;
+    dan::QkProblem p;
+    for (int s = 0; s < 2; ++s) {
+        p.q[s] = qkv[s][0];
+        p.k[s] = qkv[s][1];
+        p.v[s] = qkv[s][2];
+        p.T[s] = Ts[s];
+        p.stride[s] = strides[s];
+        p.wq[s] = w[2 * s];
+        p.wk[s] = w[2 * s + 1];
+        p.rope[s] = rope[s];
+        p.eps[s] = eps[s];
+    }
+    p.q_out = const_cast<dan_bf16 *>(a.q_out);
+    p.k_out = const_cast<dan_bf16 *>(a.k_out);
+    p.v_out = const_cast<dan_bf16 *>(a.v_out);
+    p.heads = a.heads;
+    p.head_dim = a.head_dim;
+    return launched(dan::launch_qk_norm_rope(p, neox, static_cast<cudaStream_t>(stream)));
+}
 
 } // namespace
 
@@ -442,14 +486,11 @@ int dan_can_use_qk_norm_rope_epilogue(
     const dan_bf16 *wk_img, const float *rope_txt, const float *rope_img, float eps_txt,
     float eps_img, const dan_bf16 *q_out, const dan_bf16 *k_out, const dan_bf16 *v_out)
 {
-    const dan_bf16 *const qkv[2][3] = {{q_txt, k_txt, v_txt}, {q_img, k_img, v_img}};
-    const int64_t Ts[2] = {T_txt, T_img}, strides[2] = {txt_row_stride, img_row_stride};
-    const dan_bf16 *const w[4] = {wq_txt, wk_txt, wq_img, wk_img};
-    const float *const rope[2] = {rope_txt, rope_img};
-    const float eps[2] = {eps_txt, eps_img};
-    const dan_bf16 *const outs[3] = {q_out, k_out, v_out};
-    bool empty;
-    return validate_qk(qkv, Ts, strides, heads, head_dim, w, rope, eps, outs, &empty);
+    const QkArgs a{q_txt,  k_txt,  v_txt,    T_txt,    txt_row_stride, q_img,   k_img,   v_img,
+                   T_img,  img_row_stride,   heads,    head_dim,       wq_txt,  wk_txt,  wq_img,
+                   wk_img, rope_txt,         rope_img, eps_txt,        eps_img, q_out,   k_out,
+                   v_out};
+    return qk_call(a, false, true, nullptr);
 }
 
 int dan_qk_norm_rope_epilogue(const dan_bf16 *q_txt, const dan_bf16 *k_txt, const dan_bf16 *v_txt,
@@ -462,32 +503,43 @@ int dan_qk_norm_rope_epilogue(const dan_bf16 *q_txt, const dan_bf16 *k_txt, cons
                               float eps_img, dan_bf16 *q_out, dan_bf16 *k_out, dan_bf16 *v_out,
                               void *stream)
 {
-    const dan_bf16 *const qkv[2][3] = {{q_txt, k_txt, v_txt}, {q_img, k_img, v_img}};
-    const int64_t Ts[2] = {T_txt, T_img}, strides[2] = {txt_row_stride, img_row_stride};
-    const dan_bf16 *const w[4] = {wq_txt, wk_txt, wq_img, wk_img};
-    const float *const rope[2] = {rope_txt, rope_img};
-    const float eps[2] = {eps_txt, eps_img};
-    const dan_bf16 *const outs[3] = {q_out, k_out, v_out};
-    bool empty;
-    const int st = validate_qk(qkv, Ts, strides, heads, head_dim, w, rope, eps, outs, &empty);
-    if (st != DAN_OK || empty) return st;
-    dan::QkProblem p;
-    for (int s = 0; s < 2; ++s) {
-        p.q[s] = qkv[s][0];
-        p.k[s] = qkv[s][1];
-        p.v[s] = qkv[s][2];
-        p.T[s] = Ts[s];
-        p.stride[s] = strides[s];
-        p.wq[s] = w[2 * s];
-        p.wk[s] = w[2 * s + 1];
-        p.rope[s] = rope[s];
-        p.eps[s] = eps[s];
-    }
-    p.q_out = q_out;
-    p.k_out = k_out;
-    p.v_out = v_out;
-    p.heads = heads;
-    return launched(dan::launch_qk_norm_rope_epilogue(p, static_cast<cudaStream_t>(stream)));
+    const QkArgs a{q_txt,  k_txt,  v_txt,    T_txt,    txt_row_stride, q_img,   k_img,   v_img,
+                   T_img,  img_row_stride,   heads,    head_dim,       wq_txt,  wk_txt,  wq_img,
+                   wk_img, rope_txt,         rope_img, eps_txt,        eps_img, q_out,   k_out,
+                   v_out};
+    return qk_call(a, false, false, stream);
+}
+
+int dan_can_use_qk_norm_rope_neox_epilogue(
+    const dan_bf16 *q_txt, const dan_bf16 *k_txt, const dan_bf16 *v_txt, int64_t T_txt,
+    int64_t txt_row_stride, const dan_bf16 *q_img, const dan_bf16 *k_img, const dan_bf16 *v_img,
+    int64_t T_img, int64_t img_row_stride, int64_t heads, int64_t head_dim,
+    const dan_bf16 *wq_txt, const dan_bf16 *wk_txt, const dan_bf16 *wq_img,
+    const dan_bf16 *wk_img, const float *rope_txt, const float *rope_img, float eps_txt,
+    float eps_img, const dan_bf16 *q_out, const dan_bf16 *k_out, const dan_bf16 *v_out)
+{
+    const QkArgs a{q_txt,  k_txt,  v_txt,    T_txt,    txt_row_stride, q_img,   k_img,   v_img,
+                   T_img,  img_row_stride,   heads,    head_dim,       wq_txt,  wk_txt,  wq_img,
+                   wk_img, rope_txt,         rope_img, eps_txt,        eps_img, q_out,   k_out,
+                   v_out};
+    return qk_call(a, true, true, nullptr);
+}
+
+int dan_qk_norm_rope_neox_epilogue(const dan_bf16 *q_txt, const dan_bf16 *k_txt,
+                                   const dan_bf16 *v_txt, int64_t T_txt, int64_t txt_row_stride,
+                                   const dan_bf16 *q_img, const dan_bf16 *k_img,
+                                   const dan_bf16 *v_img, int64_t T_img, int64_t img_row_stride,
+                                   int64_t heads, int64_t head_dim, const dan_bf16 *wq_txt,
+                                   const dan_bf16 *wk_txt, const dan_bf16 *wq_img,
+                                   const dan_bf16 *wk_img, const float *rope_txt,
+                                   const float *rope_img, float eps_txt, float eps_img,
+                                   dan_bf16 *q_out, dan_bf16 *k_out, dan_bf16 *v_out, void *stream)
+{
+    const QkArgs a{q_txt,  k_txt,  v_txt,    T_txt,    txt_row_stride, q_img,   k_img,   v_img,
+                   T_img,  img_row_stride,   heads,    head_dim,       wq_txt,  wk_txt,  wq_img,
+                   wk_img, rope_txt,         rope_img, eps_txt,        eps_img, q_out,   k_out,
+                   v_out};
+    return qk_call(a, true, false, stream);
 }
 
 } // extern "C"

@@ -33,6 +33,7 @@ struct QkProblem {
     float eps[2];
     void *q_out, *k_out, *v_out;
     int64_t heads;
+    int64_t head_dim; // 128 or 64
 };
 
 // Launch fn<<<grid, block, smem, s>>>(args...) with programmatic stream
@@ -62,7 +63,8 @@ cudaError_t launch_gated_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_ln_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_ln_modulate_fp8(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_gated_ln_modulate(const RowProblem &p, cudaStream_t s);
-cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &p, cudaStream_t s);
+// neox: rotate the halves' pairs (i, i + head_dim/2) instead of (2i, 2i+1).
+cudaError_t launch_qk_norm_rope(const QkProblem &p, bool neox, cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -1,22 +1,23 @@
-// dan_qk.cu -- QK-RMSNorm + interleaved RoPE + V copy epilogue for sm_103a.
+// dan_qk.cu -- QK-RMSNorm + RoPE + V copy epilogue for sm_103a.
 //
 // "PR #37123 report" (Qwen-Image FP8 QKV projection and Blackwell
 // epilogue), implementation section 3: one kernel walks the Q/K/V work of
-// the text and image token streams, normalises every 128-wide head of Q and
-// K with that stream's RMSNorm weight, rotates interleaved pairs with the
-// stream's fp32 cos/sin row, copies V, and writes joint [text, image]
-// buffers; inputs are zero-copy row-strided views of the packed QKV GEMM
-// output (section 4).
+// the text and image token streams, normalises every head of Q and K with
+// that stream's RMSNorm weight, rotates it with the stream's fp32 cos/sin
+// row, copies V, and writes joint [text, image] buffers; inputs are
+// zero-copy row-strided views of the packed QKV GEMM output (section 4).
+// The page's kernel rotates interleaved pairs (is_neox=False) at head_dim
+// 128; the same kernel also takes head_dim 64 and the neox rotation of
+// halves, the QK-norm + RoPE variants the guide lists for other DiTs.
 //
-// Work unit = (token, Q|K|V, group of up to 24 heads): one bulk copy into
-// a shared-memory ring slot, processed by one consumer warp (see
-// dan_ring.cuh for the ring).  A half-warp covers one head: lane l (0..15) owns the 16-byte fragment of
-// columns 8l..8l+7, so each head is one coalesced 256-byte load/store and
-// the two halves of a warp take adjacent heads (512 contiguous bytes).  The
-// per-token RoPE row and the stream's weight fragment are read once per unit.
-// Head RMS: each lane's 8 squares in column order, then the adjacent-pair
-// tree over the 16 lanes (xor 1,2,4,8 stays inside a half-warp), done as a
-// recursive-halving fold so that each lane ends with one head's sum.
+// Work unit = (token, Q|K|V, group of heads): one bulk copy into a
+// shared-memory slot, processed by one warp (dan_ring.cuh).  LPH = HD/8
+// lanes cover one head, lane fl owning the 16-byte fragment of columns
+// 8fl..8fl+7, so each head is one coalesced load/store and the 32/LPH head
+// slots of a warp take adjacent heads.  Head RMS: each lane's 8 squares in
+// column order, then the adjacent-pair tree over the head's LPH lanes,
+// done as a recursive-halving fold so that each lane ends with the sums of
+// 16/LPH heads.
 #include "dan_device.cuh"
 #include "dan_internal.h"
 #include "dan_ring.cuh"
@@ -33,36 +34,45 @@ struct QkParams {
     float eps[2];
     uint4 *q_out, *k_out, *v_out;
     int H;
-    int groups; // head groups of kGroup heads per (token, kind)
+    int groups; // head groups per (token, kind)
     unsigned *status;
     unsigned long long limit_ns;
 };
 
 constexpr int kQkNW = 8;  // warps per CTA (measured best among 4..16)
 constexpr int kQkSPC = 1; // slots per warp
-constexpr int kHeadsPerLane = 12;         // heads a half-warp lane holds per unit
-constexpr int kGroup = 2 * kHeadsPerLane; // heads per unit
-// A ring slot holds one unit's heads (16 fragments each) and, for Q and K,
-// the token's cos/sin row (128 fp32 = 32 fragments) behind them.
-constexpr int kSlotRope = kGroup * 16;
-constexpr int kSlot = kSlotRope + 32;
+constexpr int kHeadsPerLane = 12; // head fragments a lane holds per unit
 
-// One unit of work = (token, Q|K|V, group of up to kGroup heads), as
-// loaded registers: the head fragments plus, for Q and K, the weight
-// fragment and the token's cos/sin for this lane's four pairs.
+// Shape of the work for head_dim HD.
+template <int HD>
+struct QkShape {
+    static constexpr int LPH = HD / 8;             // lanes (and fragments) per head
+    static constexpr int GPS = 32 / LPH;           // heads per warp step
+    static constexpr int GROUP = kHeadsPerLane * GPS; // heads per unit
+    static constexpr int DATA = GROUP * LPH;       // fragments of a unit's heads (6 KB)
+    static constexpr int ROPE = HD / 4;            // fragments of a cos/sin row (HD fp32)
+    static constexpr int SLOT = DATA + 32;         // slot: heads, then the cos/sin row
+    static constexpr int LEVELS = LPH == 16 ? 4 : 3; // fold levels over the head's lanes
+    static constexpr int NK = 16 >> LEVELS;        // head sums a lane ends with
+};
+
+// One unit of work = (token, Q|K|V, group of heads), as loaded registers:
+// the head fragments plus, for Q and K, the weight fragment and the cos/sin
+// of this lane's columns (interleaved: four pairs; neox: eight columns).
 struct QkUnit {
     uint4 x[kHeadsPerLane];
     uint4 w;
-    float4 c4, s4;
+    float4 c[2], s[2];
     int64_t tok;
-    int kind, h0, s;
+    int kind, h0, s_;
 };
 
 // Unit k of a CTA whose tokens start at t0: token t0 + k / (3 * groups),
-// then Q, K, V, each split in head groups.
+// then Q, K, V, each split in head groups of GROUP heads.
+template <int HD>
 __device__ __forceinline__ void qk_unit(QkUnit &U, const QkParams &p, int64_t t0, int k)
 {
-    if (p.groups == 1) { // up to kGroup heads: one unit per (token, kind); k / 3 by a constant
+    if (p.groups == 1) { // one unit per (token, kind); k / 3 by a constant
         const unsigned uk = (unsigned)k;
         U.tok = t0 + uk / 3u;
         U.kind = (int)(uk % 3u);
@@ -72,69 +82,95 @@ __device__ __forceinline__ void qk_unit(QkUnit &U, const QkParams &p, int64_t t0
         U.tok = t0 + k / per_tok;
         const int rem = k % per_tok;
         U.kind = rem / p.groups;
-        U.h0 = (rem % p.groups) * kGroup;
+        U.h0 = (rem % p.groups) * QkShape<HD>::GROUP;
     }
-    U.s = U.tok < p.T0 ? 0 : 1;
+    U.s_ = U.tok < p.T0 ? 0 : 1;
 }
 
+template <int HD>
 __device__ __forceinline__ const uint4 *qk_src(const QkUnit &U, const QkParams &p)
 {
-    const int64_t t = U.s ? U.tok - p.T0 : U.tok;
-    return (U.kind == 0 ? p.q[U.s] : U.kind == 1 ? p.k[U.s] : p.v[U.s]) + t * p.stride8[U.s] +
-           U.h0 * 16;
+    const int64_t t = U.s_ ? U.tok - p.T0 : U.tok;
+    return (U.kind == 0 ? p.q[U.s_] : U.kind == 1 ? p.k[U.s_] : p.v[U.s_]) + t * p.stride8[U.s_] +
+           U.h0 * QkShape<HD>::LPH;
 }
 
+template <int HD>
 __device__ __forceinline__ int qk_heads(const QkUnit &U, const QkParams &p)
 {
-    return p.H - U.h0 < kGroup ? p.H - U.h0 : kGroup;
+    constexpr int G = QkShape<HD>::GROUP;
+    return p.H - U.h0 < G ? p.H - U.h0 : G;
 }
 
+template <int HD>
 __device__ __forceinline__ const float4 *qk_rope_row(const QkUnit &U, const QkParams &p)
 {
-    const int64_t t = U.s ? U.tok - p.T0 : U.tok;
-    return p.rope[U.s] + t * 32;
+    const int64_t t = U.s_ ? U.tok - p.T0 : U.tok;
+    return p.rope[U.s_] + t * QkShape<HD>::ROPE;
 }
 
-// Copy the unit's heads from its ring slot into registers, with, for Q and
-// K, the stream's weight fragment (staged in s_w: wq_txt, wk_txt, wq_img,
-// wk_img) and the token's cos/sin for this lane's four pairs (in the slot).
+// Copy the unit's heads from its slot into registers, with, for Q and K,
+// the stream's weight fragment (staged in s_w: wq_txt, wk_txt, wq_img,
+// wk_img) and this lane's cos/sin (in the slot).
+template <int HD, bool NEOX>
 __device__ __forceinline__ void qk_take(QkUnit &U, const QkParams &p, const uint4 *slot,
-                                        const uint4 *s_w, int half, int fl)
+                                        const uint4 *s_w, int hs, int fl)
 {
-    const int nh = qk_heads(U, p);
+    using S = QkShape<HD>;
+    const int nh = qk_heads<HD>(U, p);
 #pragma unroll
     for (int k = 0; k < kHeadsPerLane; ++k) {
-        const int hh = half + 2 * k;
-        U.x[k] = hh < nh ? slot[hh * 16 + fl] : make_uint4(0, 0, 0, 0);
+        const int hh = hs + S::GPS * k;
+        U.x[k] = hh < nh ? slot[hh * S::LPH + fl] : make_uint4(0, 0, 0, 0);
     }
     if (U.kind != 2) {
-        U.w = s_w[(2 * U.s + U.kind) * 16 + fl];
-        const float4 *rope = reinterpret_cast<const float4 *>(slot + kSlotRope);
-        U.c4 = rope[fl];      // cos of pairs 4fl..4fl+3
-        U.s4 = rope[16 + fl]; // sin of the same pairs
+        U.w = s_w[(2 * U.s_ + U.kind) * S::LPH + fl];
+        const float4 *rope = reinterpret_cast<const float4 *>(slot + S::DATA);
+        if (NEOX) { // columns i = 8 (fl mod LPH/2) + e of the first half
+            const int b = 2 * (fl % (S::LPH / 2));
+            U.c[0] = rope[b];
+            U.c[1] = rope[b + 1];
+            U.s[0] = rope[S::ROPE / 2 + b];
+            U.s[1] = rope[S::ROPE / 2 + b + 1];
+        } else {                     // pairs 4fl .. 4fl+3
+            U.c[0] = rope[fl];
+            U.s[0] = rope[S::ROPE / 2 + fl];
+        }
     }
 }
 
-// Reverse the 4 low bits: after the halving fold, lane l holds head brev4(l).
-__device__ __forceinline__ int brev4(int l)
+// Reverse the low L bits of l.
+template <int L>
+__device__ __forceinline__ int brev(int l)
 {
-    return ((l & 1) << 3) | ((l & 2) << 1) | ((l & 4) >> 1) | ((l & 8) >> 3);
+    int r = 0;
+#pragma unroll
+    for (int i = 0; i < L; ++i) r |= ((l >> i) & 1) << (L - 1 - i);
+    return r;
 }
 
-__device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, int half, int fl)
+__device__ __forceinline__ float f4(const float4 &v, int i)
 {
-    uint4 *dst = (U.kind == 0 ? p.q_out : U.kind == 1 ? p.k_out : p.v_out) + U.tok * p.H * 16;
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <int HD, bool NEOX>
+__device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, int hs, int fl)
+{
+    using S = QkShape<HD>;
+    uint4 *dst = (U.kind == 0 ? p.q_out : U.kind == 1 ? p.k_out : p.v_out) +
+                 U.tok * p.H * S::LPH;
     if (U.kind == 2) { // V: bit copy
 #pragma unroll
         for (int k = 0; k < kHeadsPerLane; ++k) {
-            const int h = U.h0 + half + 2 * k;
-            if (h < p.H) st_stream(dst + h * 16 + fl, U.x[k]);
+            const int h = U.h0 + hs + S::GPS * k;
+            if (h < p.H) st_stream(dst + h * S::LPH + fl, U.x[k]);
         }
         return;
     }
 
-    // The lane's columns widened to fp32 once; packed operations take the
-    // two columns of one rotation pair (2i, 2i+1) throughout.
+    // The lane's columns widened to fp32 once; packed operations take two
+    // neighbouring columns throughout.
     float x[kHeadsPerLane][8];
 #pragma unroll
     for (int k = 0; k < kHeadsPerLane; ++k)
@@ -163,13 +199,12 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
 #pragma unroll
     for (int k = kHeadsPerLane; k < 16; ++k) ps[k] = 0.0f;
 
-    // Recursive-halving fold over the 16 lanes of the half-warp: at xor
-    // offset 1, 2, 4, 8 each lane keeps half of its heads and adds its
-    // partner's partial for them.  Per head this is exactly the adjacent-pair
-    // tree over the 16 lanes; afterwards lane fl holds the sum of head
-    // brev4(fl), so each lane computes one reciprocal square root.
+    // Recursive-halving fold over the head's LPH lanes: at xor offset 1, 2,
+    // .. each lane keeps half of its entries and adds its partner's partial
+    // for them.  Per head this is exactly the adjacent-pair tree over the
+    // lanes; afterwards lane fl holds the sums of heads NK*brev(fl) + j.
 #pragma unroll
-    for (int lvl = 0, n = 16; lvl < 4; ++lvl, n >>= 1) {
+    for (int lvl = 0, n = 16; lvl < S::LEVELS; ++lvl, n >>= 1) {
         const int off = 1 << lvl;
         const bool upper = (fl & off) != 0;
 #pragma unroll
@@ -179,54 +214,84 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
             ps[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
         }
     }
-    const float my_rstd = defined_rsqrt(__fadd_rn(__fdiv_rn(ps[0], 128.0f), p.eps[U.s]));
-
-    // cos and sin of the lane's four pairs, each duplicated for a packed
-    // multiply of both members (a, b) of a pair.
-    const float cs[4] = {U.c4.x, U.c4.y, U.c4.z, U.c4.w};
-    const float sn[4] = {U.s4.x, U.s4.y, U.s4.z, U.s4.w};
-    float2 cc[4], ss[4], w2[4];
+    float my_rstd[S::NK];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        cc[m] = dup2(cs[m]);
-        ss[m] = dup2(sn[m]);
-        w2[m] = wide2(word(U.w, m));
+    for (int j = 0; j < S::NK; ++j)
+        my_rstd[j] = defined_rsqrt(__fadd_rn(__fdiv_rn(ps[j], (float)HD), p.eps[U.s_]));
+
+    float2 w2[4], cc[4], sn[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) w2[m] = wide2(word(U.w, m));
+    const bool first = fl < S::LPH / 2; // neox: the lane holds the first half's columns
+    if (NEOX) {
+        // columns (2m, 2m+1) of the lane: cos pairs and sin pairs, the sin
+        // negated in the first half so both halves add: out = own*c + other*s'
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float4 &c4 = U.c[m / 2], &s4 = U.s[m / 2];
+            cc[m] = make_float2(f4(c4, 2 * (m % 2)), f4(c4, 2 * (m % 2) + 1));
+            const float2 s2 = make_float2(f4(s4, 2 * (m % 2)), f4(s4, 2 * (m % 2) + 1));
+            sn[m] = first ? make_float2(-s2.x, -s2.y) : s2;
+        }
+    } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            cc[m] = dup2(f4(U.c[0], m));
+            sn[m] = dup2(f4(U.s[0], m));
+        }
     }
-    const int lane_base = half << 4;
+    const int lane_base = hs * S::LPH;
 #pragma unroll
     for (int k = 0; k < kHeadsPerLane; ++k) {
-        const float rstd = __shfl_sync(kFull, my_rstd, lane_base + brev4(k));
-        if (U.h0 + 2 * k >= p.H) break; // warp-uniform: no head left for either half
-        const int h = U.h0 + half + 2 * k;
+        const float rstd = __shfl_sync(kFull, my_rstd[k % S::NK], lane_base + brev<S::LEVELS>(k / S::NK));
+        if (U.h0 + S::GPS * k >= p.H) break; // warp-uniform: no head left in any slot
+        const int h = U.h0 + hs + S::GPS * k;
         const float2 r2 = dup2(rstd);
-        uint4 out;
+        uint32_t nw[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) { // pair i = 4fl + m: columns 2i, 2i+1
+        for (int m = 0; m < 4; ++m) {
             const float2 t2 = mul2(mul2(make_float2(x[k][2 * m], x[k][2 * m + 1]), r2), w2[m]);
-            const float2 ab = wide2(pack_bf16(t2.x, t2.y)); // (a, b) rounded to bf16
-            const float2 pc = mul2(ab, cc[m]);              // (rn(a c), rn(b c))
-            const float2 ps2 = mul2(ab, ss[m]);             // (rn(a s), rn(b s))
-            set_word(out, m, pack_bf16(__fsub_rn(pc.x, ps2.y), __fadd_rn(ps2.x, pc.y)));
+            nw[m] = pack_bf16(t2.x, t2.y); // normalised, rounded to bf16
         }
-        if (h < p.H) st_stream(dst + h * 16 + fl, out);
+        uint4 out;
+        if (NEOX) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t other = __shfl_xor_sync(kFull, nw[m], S::LPH / 2);
+                const float2 xc = mul2(wide2(nw[m]), cc[m]);  // rn(own * c)
+                const float2 ys = mul2(wide2(other), sn[m]);  // rn(other * (-+ s))
+                set_word(out, m, pack_bf16(__fadd_rn(xc.x, ys.x), __fadd_rn(xc.y, ys.y)));
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) { // pair i = 4fl + m: columns 2i, 2i+1
+                const float2 ab = wide2(nw[m]);       // (a, b)
+                const float2 pc = mul2(ab, cc[m]);    // (rn(a c), rn(b c))
+                const float2 ps2 = mul2(ab, sn[m]);   // (rn(a s), rn(b s))
+                set_word(out, m, pack_bf16(__fsub_rn(pc.x, ps2.y), __fadd_rn(ps2.x, pc.y)));
+            }
+        }
+        if (h < p.H) st_stream(dst + h * S::LPH + fl, out);
     }
 }
 
 // CTA c takes the contiguous tokens [c*T/G, (c+1)*T/G); its warp w takes
 // the CTA's units w, w + kQkNW, ... and requests each kQkSPC units ahead
-// into its own 6.5 KB slots (dan_ring.cuh): one bulk copy of the unit's
-// heads, plus one of the token's cos/sin row for Q and K.  The four
-// 256-byte weight vectors are staged in shared memory once per CTA.
+// into its own slots (dan_ring.cuh): one bulk copy of the unit's heads,
+// plus one of the token's cos/sin row for Q and K.  The four weight
+// vectors are staged in shared memory once per CTA.
+template <int HD, bool NEOX>
 __global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkParams p)
 {
+    using S = QkShape<HD>;
     using Pipe = WarpPipe<kQkSPC>;
     extern __shared__ __align__(128) uint4 smem[];
     uint4 *ring = smem;
-    uint4 *s_w = ring + kQkNW * kQkSPC * kSlot; // 4 x 16 fragments
-    uint64_t *full = reinterpret_cast<uint64_t *>(s_w + 64);
+    uint4 *s_w = ring + kQkNW * kQkSPC * S::SLOT; // 4 x LPH fragments
+    uint64_t *full = reinterpret_cast<uint64_t *>(s_w + 4 * S::LPH);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = (lane >> 4) & 1, fl = lane & 15;
+    const int hs = lane / S::LPH, fl = lane % S::LPH;
     const int64_t G = gridDim.x;
     const int64_t t0 = (int64_t)blockIdx.x * p.T_all / G;
     const int64_t t1 = (int64_t)(blockIdx.x + 1) * p.T_all / G;
@@ -238,29 +303,29 @@ __global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkPar
     }
     grid_dependency_wait(); // no global access above this line
     allow_dependents();
-    if (threadIdx.x < 64) { // the weights of a stream with no tokens are never read
-        const int v = threadIdx.x >> 4, s = v >> 1;
+    if (threadIdx.x < 4 * S::LPH) { // the weights of a stream with no tokens are never read
+        const int v = threadIdx.x / S::LPH, s = v >> 1;
         if (s == 0 ? p.T0 > 0 : p.T_all > p.T0)
-            s_w[threadIdx.x] = ld_vec((v & 1 ? p.wk[s] : p.wq[s]) + (threadIdx.x & 15));
+            s_w[threadIdx.x] = ld_vec((v & 1 ? p.wk[s] : p.wq[s]) + (threadIdx.x % S::LPH));
     }
     __syncthreads(); // barriers initialised, weights staged
 
-    uint4 *slots = ring + warp * kQkSPC * kSlot;
+    uint4 *slots = ring + warp * kQkSPC * S::SLOT;
     uint64_t *bar = full + warp * kQkSPC;
     const int units = warp < n ? (n - warp + kQkNW - 1) / kQkNW : 0;
     auto request = [&](int i) { // lane 0 only
         QkUnit U;
-        qk_unit(U, p, t0, warp + kQkNW * i);
-        const unsigned bytes = (unsigned)qk_heads(U, p) * 256u;
-        uint4 *slot = slots + Pipe::slot(i) * kSlot;
+        qk_unit<HD>(U, p, t0, warp + kQkNW * i);
+        const unsigned bytes = (unsigned)qk_heads<HD>(U, p) * (unsigned)(HD * 2);
+        uint4 *slot = slots + Pipe::slot(i) * S::SLOT;
         uint64_t *b = bar + Pipe::slot(i);
         if (U.kind == 2) {
             mbar_arrive_expect_tx(b, bytes);
-            bulk_load(slot, qk_src(U, p), bytes, b);
+            bulk_load(slot, qk_src<HD>(U, p), bytes, b);
         } else {
-            mbar_arrive_expect_tx(b, bytes + 512u);
-            bulk_load(slot, qk_src(U, p), bytes, b);
-            bulk_load(slot + kSlotRope, qk_rope_row(U, p), 512u, b);
+            mbar_arrive_expect_tx(b, bytes + HD * 4u);
+            bulk_load(slot, qk_src<HD>(U, p), bytes, b);
+            bulk_load(slot + S::DATA, qk_rope_row<HD>(U, p), HD * 4u, b);
         }
     };
     if (lane == 0)
@@ -272,15 +337,33 @@ __global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkPar
             return;
         }
         QkUnit U;
-        qk_unit(U, p, t0, warp + kQkNW * i);
-        qk_take(U, p, slots + Pipe::slot(i) * kSlot, s_w, half, fl);
+        qk_unit<HD>(U, p, t0, warp + kQkNW * i);
+        qk_take<HD, NEOX>(U, p, slots + Pipe::slot(i) * S::SLOT, s_w, hs, fl);
         slot_reads_done();
         if (lane == 0 && i + kQkSPC < units) request(i + kQkSPC);
-        qk_process(U, p, half, fl);
+        qk_process<HD, NEOX>(U, p, hs, fl);
     }
 }
 
-cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &q, cudaStream_t s)
+namespace {
+
+template <int HD, bool NEOX>
+cudaError_t launch_qk(QkParams p, int64_t heads, cudaStream_t s)
+{
+    using S = QkShape<HD>;
+    p.groups = (int)((heads + S::GROUP - 1) / S::GROUP);
+    constexpr int NS = kQkNW * kQkSPC;
+    const int smem = NS * S::SLOT * 16 + 4 * S::LPH * 16 + NS * 8;
+    auto fn = qk_norm_rope_kernel<HD, NEOX>;
+    const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(fn), smem);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)(p.T_all < sm_count() ? p.T_all : sm_count());
+    return launch_overlapped(fn, grid, 32 * kQkNW, smem, s, p);
+}
+
+} // namespace
+
+cudaError_t launch_qk_norm_rope(const QkProblem &q, bool neox, cudaStream_t s)
 {
     QkParams p;
     for (int i = 0; i < 2; ++i) {
@@ -299,16 +382,12 @@ cudaError_t launch_qk_norm_rope_epilogue(const QkProblem &q, cudaStream_t s)
     p.k_out = static_cast<uint4 *>(q.k_out);
     p.v_out = static_cast<uint4 *>(q.v_out);
     p.H = (int)q.heads;
-    p.groups = (int)((q.heads + kGroup - 1) / kGroup);
+    p.groups = 0;
     p.status = device_status();
     p.limit_ns = 1000000000ull;
-
-    constexpr int S = kQkNW * kQkSPC;
-    const int smem = S * kSlot * 16 + 64 * 16 + S * 8;
-    const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(qk_norm_rope_kernel), smem);
-    if (e != cudaSuccess) return e;
-    const int grid = (int)(p.T_all < sm_count() ? p.T_all : sm_count());
-    return launch_overlapped(qk_norm_rope_kernel, grid, 32 * kQkNW, smem, s, p);
+    if (q.head_dim == 64)
+        return neox ? launch_qk<64, true>(p, q.heads, s) : launch_qk<64, false>(p, q.heads, s);
+    return neox ? launch_qk<128, true>(p, q.heads, s) : launch_qk<128, false>(p, q.heads, s);
 }
 
 } // namespace dan

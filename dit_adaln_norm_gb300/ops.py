@@ -41,6 +41,10 @@ _SIGS = {
                                   _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P],
     "dan_can_use_qk_norm_rope_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
                                           _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P],
+    "dan_qk_norm_rope_neox_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
+                                       _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P, _P],
+    "dan_can_use_qk_norm_rope_neox_epilogue": [_P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I,
+                                               _P, _P, _P, _P, _P, _P, _F, _F, _P, _P, _P],
 }
 
 _lib = None
@@ -219,41 +223,46 @@ def ln_modulate_fp8(x, scale, shift, qscale: float, eps: float, out=None):
     return q
 
 
-def _qkv(views, name, heads):
+def _qkv(views, name, heads, hd):
     q, k, v = views
     T = q.shape[0]
     for t, n in zip(views, "qkv"):
         _bf16_cuda(t, f"{name}.{n}")
-        if t.dim() != 2 or t.shape != (T, heads * 128) or (T > 0 and t.stride(1) != 1):
-            raise ValueError(f"{name}.{n}: expected a [T, heads*128] view with unit column stride")
-    strides = {t.stride(0) for t in views} if T > 1 else {heads * 128}
+        if t.dim() != 2 or t.shape != (T, heads * hd) or (T > 0 and t.stride(1) != 1):
+            raise ValueError(f"{name}.{n}: expected a [T, heads*{hd}] view with unit column stride")
+    strides = {t.stride(0) for t in views} if T > 1 else {heads * hd}
     if len(strides) != 1:
         raise ValueError(f"{name}: q, k, v must share one row stride")
     return T, strides.pop()
 
 
 def qk_norm_rope_epilogue(txt, img, wq_txt, wk_txt, wq_img, wk_img, rope_txt, rope_img,
-                          eps_txt: float, eps_img: float, heads: int, out=None):
-    """txt, img: (q, k, v) views [T_s, heads*128]; weights [128] bf16; rope
-    tables fp32 [T_s, 128].  Returns joint (q, k, v), each [T_txt+T_img, heads, 128]."""
-    Tt, st = _qkv(txt, "txt", heads)
-    Ti, si = _qkv(img, "img", heads)
+                          eps_txt: float, eps_img: float, heads: int, out=None,
+                          head_dim: int = 128, neox: bool = False):
+    """txt, img: (q, k, v) views [T_s, heads*head_dim]; weights [head_dim] bf16;
+    rope tables fp32 [T_s, head_dim].  Returns joint (q, k, v), each
+    [T_txt+T_img, heads, head_dim].  head_dim 128 or 64; neox=True rotates
+    the halves' pairs (dan_qk_norm_rope_neox_epilogue) instead of
+    interleaved pairs."""
+    hd = int(head_dim)
+    Tt, st = _qkv(txt, "txt", heads, hd)
+    Ti, si = _qkv(img, "img", heads, hd)
     for w, n in ((wq_txt, "wq_txt"), (wk_txt, "wk_txt"), (wq_img, "wq_img"), (wk_img, "wk_img")):
         _bf16_cuda(w, n)
-        if w.shape != (128,) or not w.is_contiguous():
-            raise ValueError(f"{n}: expected a contiguous [128] tensor")
+        if w.shape != (hd,) or not w.is_contiguous():
+            raise ValueError(f"{n}: expected a contiguous [{hd}] tensor")
     for r, n, T in ((rope_txt, "rope_txt", Tt), (rope_img, "rope_img", Ti)):
-        if not r.is_cuda or r.dtype != torch.float32 or r.shape != (T, 128) or not r.is_contiguous():
-            raise ValueError(f"{n}: expected a contiguous CUDA float32 [T, 128] tensor")
+        if not r.is_cuda or r.dtype != torch.float32 or r.shape != (T, hd) or not r.is_contiguous():
+            raise ValueError(f"{n}: expected a contiguous CUDA float32 [T, {hd}] tensor")
     if out is None:
         dev = txt[0].device
-        out = tuple(torch.empty((Tt + Ti, heads, 128), dtype=torch.bfloat16, device=dev)
+        out = tuple(torch.empty((Tt + Ti, heads, hd), dtype=torch.bfloat16, device=dev)
                     for _ in range(3))
     qo, ko, vo = out
-    _check(load().dan_qk_norm_rope_epilogue(
+    name = "dan_qk_norm_rope_neox_epilogue" if neox else "dan_qk_norm_rope_epilogue"
+    _check(getattr(load(), name)(
         _ptr(txt[0]), _ptr(txt[1]), _ptr(txt[2]), Tt, st,
-        _ptr(img[0]), _ptr(img[1]), _ptr(img[2]), Ti, si, heads, 128,
+        _ptr(img[0]), _ptr(img[1]), _ptr(img[2]), Ti, si, heads, hd,
         _ptr(wq_txt), _ptr(wk_txt), _ptr(wq_img), _ptr(wk_img), _ptr(rope_txt), _ptr(rope_img),
-        float(eps_txt), float(eps_img), _ptr(qo), _ptr(ko), _ptr(vo), _stream()),
-        "dan_qk_norm_rope_epilogue")
+        float(eps_txt), float(eps_img), _ptr(qo), _ptr(ko), _ptr(vo), _stream()), name)
     return qo, ko, vo

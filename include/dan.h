@@ -1,7 +1,7 @@
 /*
  * dan.h -- C ABI of the GB300 (sm_103a) fused adaLN norm+modulate kernels.
  *
- * Six operations, each a single kernel launch on the caller's stream:
+ * Seven operations, each a single kernel launch on the caller's stream:
  *
  *   dan_ln_modulate         y = bf16(LayerNorm(x) * (1 + scale) + shift)
  *   dan_ln_modulate_fp8     q = e4m3(y * rn(1/qscale)), y as dan_ln_modulate
@@ -10,6 +10,7 @@
  *   dan_gated_rms_modulate  r' = bf16(r + bf16(gate * h)); y = rms_modulate(r')
  *   dan_qk_norm_rope_epilogue  per-head RMSNorm + interleaved RoPE of Q and K,
  *                           copy of V, into joint [text, image] buffers
+ *   dan_qk_norm_rope_neox_epilogue  the same with the neox rotation of halves
  *
  * The operations are the ones described on these pages:
  *  - "SGLang diffusion fused-op package guide", section "Norm + scale/shift
@@ -213,23 +214,24 @@ int dan_can_use_ln_modulate_fp8(const dan_bf16 *x, const dan_bf16 *scale, const 
 
 /* ------------------------------------------- QK-RMSNorm + RoPE epilogue
  * Two token streams (text, then image), each given as three row-strided
- * views q, k, v of [T_s, heads*128] bf16 that share one row stride
- * (`*_row_stride` elements, >= heads*128, a multiple of 8; e.g. the column
- * slices of a packed [T_s, 3*heads*128] QKV GEMM output, or separate
- * contiguous tensors).  Heads are contiguous 128-element blocks.
+ * views q, k, v of [T_s, heads*hd] bf16 (hd = head_dim, 128 or 64) that
+ * share one row stride (`*_row_stride` elements, >= heads*hd, a multiple of
+ * 8; e.g. the column slices of a packed [T_s, 3*heads*hd] QKV GEMM output,
+ * or separate contiguous tensors).  Heads are contiguous hd-element blocks.
  * For every token t and head h of Q and of K:
- *   rstd = rn(1/rn(sqrt(rn(rn(s/128) + eps_stream)))), s folded from 16
+ *   rstd = rn(1/rn(sqrt(rn(rn(s/hd) + eps_stream)))), s folded from hd/8
  *          logical threads (thread l sums columns 8l..8l+7 in order) by the
  *          adjacent-pair tree,
- *   n_j  = bf16(rn(rn(x_j * rstd) * w_j))   (w: that stream's q or k weight [128])
+ *   n_j  = bf16(rn(rn(x_j * rstd) * w_j))   (w: that stream's q or k weight [hd])
  *   out_{2i}   = bf16(rn(rn(n_{2i} * c_i) - rn(n_{2i+1} * s_i)))
  *   out_{2i+1} = bf16(rn(rn(n_{2i} * s_i) + rn(n_{2i+1} * c_i)))
- * with c_i = rope[t][i], s_i = rope[t][64 + i] (fp32 rows [cos_0..63 | sin_0..63]
- * of that stream's table, row stride 128).  V heads are copied unchanged.
- * Outputs q_out, k_out, v_out are contiguous [T_txt + T_img, heads, 128],
- * text tokens first.  head_dim must be 128 (DAN_EUNSUPPORTED otherwise);
- * heads >= 1; T_txt, T_img >= 0; a stream with T_s == 0 may pass NULL
- * pointers for its inputs. */
+ * (interleaved pairs, the Qwen epilogue's is_neox=False) with c_i =
+ * rope[t][i], s_i = rope[t][hd/2 + i] (fp32 rows [cos_0..cos_{hd/2-1} |
+ * sin_0..] of that stream's table, row stride hd).  V heads are copied
+ * unchanged.  Outputs q_out, k_out, v_out are contiguous
+ * [T_txt + T_img, heads, hd], text tokens first.  head_dim 128 or 64
+ * (DAN_EUNSUPPORTED otherwise); heads >= 1; T_txt, T_img >= 0; a stream
+ * with T_s == 0 may pass NULL pointers for its inputs. */
 int dan_qk_norm_rope_epilogue(const dan_bf16 *q_txt, const dan_bf16 *k_txt, const dan_bf16 *v_txt,
                               int64_t T_txt, int64_t txt_row_stride, const dan_bf16 *q_img,
                               const dan_bf16 *k_img, const dan_bf16 *v_img, int64_t T_img,
@@ -240,6 +242,30 @@ int dan_qk_norm_rope_epilogue(const dan_bf16 *q_txt, const dan_bf16 *k_txt, cons
                               float eps_img, dan_bf16 *q_out, dan_bf16 *k_out, dan_bf16 *v_out,
                               void *stream);
 int dan_can_use_qk_norm_rope_epilogue(
+    const dan_bf16 *q_txt, const dan_bf16 *k_txt, const dan_bf16 *v_txt, int64_t T_txt,
+    int64_t txt_row_stride, const dan_bf16 *q_img, const dan_bf16 *k_img, const dan_bf16 *v_img,
+    int64_t T_img, int64_t img_row_stride, int64_t heads, int64_t head_dim,
+    const dan_bf16 *wq_txt, const dan_bf16 *wk_txt, const dan_bf16 *wq_img,
+    const dan_bf16 *wk_img, const float *rope_txt, const float *rope_img, float eps_txt,
+    float eps_img, const dan_bf16 *q_out, const dan_bf16 *k_out, const dan_bf16 *v_out);
+
+/* The same epilogue with the neox rotation of halves ("rotate half"): for
+ * i < hd/2 the pair is (i, i + hd/2),
+ *   out_i        = bf16(rn(rn(n_i * c_i) - rn(n_{i+hd/2} * s_i)))
+ *   out_{i+hd/2} = bf16(rn(rn(n_i * s_i) + rn(n_{i+hd/2} * c_i)))
+ * with the same table rows; everything else as dan_qk_norm_rope_epilogue.
+ * The guide lists QK-norm + RoPE variants for other DiTs (FLUX.2, ERNIE);
+ * this is the rotation they use when is_neox is set. */
+int dan_qk_norm_rope_neox_epilogue(const dan_bf16 *q_txt, const dan_bf16 *k_txt,
+                                   const dan_bf16 *v_txt, int64_t T_txt, int64_t txt_row_stride,
+                                   const dan_bf16 *q_img, const dan_bf16 *k_img,
+                                   const dan_bf16 *v_img, int64_t T_img, int64_t img_row_stride,
+                                   int64_t heads, int64_t head_dim, const dan_bf16 *wq_txt,
+                                   const dan_bf16 *wk_txt, const dan_bf16 *wq_img,
+                                   const dan_bf16 *wk_img, const float *rope_txt,
+                                   const float *rope_img, float eps_txt, float eps_img,
+                                   dan_bf16 *q_out, dan_bf16 *k_out, dan_bf16 *v_out, void *stream);
+int dan_can_use_qk_norm_rope_neox_epilogue(
     const dan_bf16 *q_txt, const dan_bf16 *k_txt, const dan_bf16 *v_txt, int64_t T_txt,
     int64_t txt_row_stride, const dan_bf16 *q_img, const dan_bf16 *k_img, const dan_bf16 *v_img,
     int64_t T_img, int64_t img_row_stride, int64_t heads, int64_t head_dim,

@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = ops.declared_symbols()
-    assert len(names) == 16
+    assert len(names) == 18
     for n in names:
         assert hasattr(lib, n), n
 
@@ -130,7 +130,7 @@ def test_qk_validation(lib):
             wt, wt + 256, wt + 512, wt + 768, rt, ri, eps_t, eps_i, qo, ko, vo)
 
     assert f() == OK
-    assert f(hd=64) == EUNSUP
+    assert f(hd=96) == EUNSUP and f(hd=256) == EUNSUP
     assert f(heads=0) == EINVAL and f(Tt=-1) == EINVAL
     assert f(st=Hh * 128) == OK            # contiguous q/k/v views of separate width
     assert f(st=Hh * 128 - 8) == EINVAL     # stride shorter than a row
@@ -141,6 +141,21 @@ def test_qk_validation(lib):
     assert f(vo=QI + 64) == EALIAS          # output over an input
     assert f(Tt=0, qt=None) == OK           # an empty text stream may pass NULL
     assert f(Tt=0, Ti=0, qt=None, qi=None) == OK
+    assert f(hd=64) == OK                  # head_dim 64: rows of 24 x 64 fit the same strides
+
+
+def test_qk_neox_validation_matches(lib):
+    QT, QI, WT, RT, RI, QO, KO, VO = (0x10000000 + i * 256 * MB for i in range(8))
+    for hd, heads in ((128, 24), (64, 48)):
+        S = 3 * heads * hd
+        w = heads * hd * 2
+        args = (QT, QT + w, QT + 2 * w, 256, S, QI, QI + w, QI + 2 * w, 4096, S, heads, hd,
+                WT, WT + 256, WT + 512, WT + 768, RT, RI, EPS, EPS, QO, KO, VO)
+        assert lib.dan_can_use_qk_norm_rope_neox_epilogue(*args) == OK
+        assert lib.dan_can_use_qk_norm_rope_epilogue(*args) == OK
+    bad = (QT, QT, QT, 1, 128, None, None, None, 0, 0, 1, 32, WT, WT, WT, WT, RT, RI, EPS, EPS,
+           QO, KO, VO)
+    assert lib.dan_can_use_qk_norm_rope_neox_epilogue(*bad) == EUNSUP
 
 
 def test_binding_raises_without_cuda_tensors():

@@ -241,28 +241,29 @@ def test_invalid_arguments_raise_before_launch():
 
 # ------------------------------------------------------- QK epilogue
 
-def run_qk(Tt, Ti, H, seed, packed=True, eps=(1e-6, 1e-6)):
-    pt = synth.packed_qkv(Tt, H, seed)
-    pi = synth.packed_qkv(Ti, H, seed + 1)
-    ws = synth.head_weights(4, seed + 2)
-    rt, ri = synth.rope_table(Tt), synth.rope_table(Ti, pos0=Tt)
+def run_qk(Tt, Ti, H, seed, packed=True, eps=(1e-6, 1e-6), hd=128, neox=False):
+    pt = synth.packed_qkv(Tt, H, seed, hd)
+    pi = synth.packed_qkv(Ti, H, seed + 1, hd)
+    ws = synth.head_weights(4, seed + 2, hd)
+    rt, ri = synth.rope_table(Tt, hd), synth.rope_table(Ti, hd, pos0=Tt)
     if packed:
         Pt, Pi = to_dev(pt), to_dev(pi)
-        dt, di = synth.split_qkv(Pt, H), synth.split_qkv(Pi, H)
+        dt, di = synth.split_qkv(Pt, H, hd), synth.split_qkv(Pi, H, hd)
     else:
-        dt = tuple(to_dev(a) for a in synth.split_qkv(pt, H))
-        di = tuple(to_dev(a) for a in synth.split_qkv(pi, H))
+        dt = tuple(to_dev(a) for a in synth.split_qkv(pt, H, hd))
+        di = tuple(to_dev(a) for a in synth.split_qkv(pi, H, hd))
     dw = [to_dev(w) for w in ws]
-    bufs, outs = zip(*[guarded((Tt + Ti, H, 128)) for _ in range(3)])
+    bufs, outs = zip(*[guarded((Tt + Ti, H, hd)) for _ in range(3)])
     ops.qk_norm_rope_epilogue(dt, di, *dw, torch.from_numpy(rt).cuda(),
-                              torch.from_numpy(ri).cuda(), eps[0], eps[1], H, out=outs)
+                              torch.from_numpy(ri).cuda(), eps[0], eps[1], H, out=outs,
+                              head_dim=hd, neox=neox)
     torch.cuda.synchronize()
     for b in bufs:
         check_guard(b)
-    want = oracle.qk_norm_rope_epilogue(synth.split_qkv(pt, H), synth.split_qkv(pi, H), H, ws,
-                                        rt, ri, eps[0], eps[1])
+    want = oracle.qk_norm_rope_epilogue(synth.split_qkv(pt, H, hd), synth.split_qkv(pi, H, hd),
+                                        H, ws, rt, ri, eps[0], eps[1], head_dim=hd, neox=neox)
     for name, g, w in zip("qkv", outs, want):
-        assert_bits_equal(from_dev(g), w, f"qk {name} Tt={Tt} Ti={Ti} H={H}")
+        assert_bits_equal(from_dev(g), w, f"qk {name} Tt={Tt} Ti={Ti} H={H} hd={hd} neox={neox}")
 
 
 @pytest.mark.parametrize("H", [24, 3, 1, 30])
@@ -279,6 +280,17 @@ def test_qk_one_stream_empty():
 def test_qk_config():
     """Qwen-Image packed QKV: 256 text + 4096 image tokens, 24 heads x 128."""
     run_qk(256, 4096, 24, synth.SEED_X)
+
+
+@pytest.mark.parametrize("hd,neox", [(64, False), (64, True), (128, True)])
+@pytest.mark.parametrize("H", [1, 5, 24, 48, 50])
+def test_qk_variants_small(hd, neox, H):
+    run_qk(5, 29, H, 620 + H + hd, packed=H % 2 == 0, eps=(1e-6, 1e-5), hd=hd, neox=neox)
+
+
+@pytest.mark.parametrize("hd,neox", [(64, False), (64, True), (128, True)])
+def test_qk_variants_config(hd, neox):
+    run_qk(256, 4096, 24 if hd == 128 else 48, synth.SEED_X + 7, hd=hd, neox=neox)
 
 
 def test_signed_zeros_through_the_modulate_chain():
