@@ -23,6 +23,8 @@ Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``
   permutation of the interleaved one, fp64 brute force.
 * ``gated_ln_modulate``: pinned (r' against an independent elementwise
   formula, gate = 0 and the composition with ``ln_modulate`` of r').
+* ``gated_residual_transposed``: pinned (torch bf16 ops on the transposed
+  update, gate = 0 and gate = 1).
 * ``fp8_e4m3``: pinned (every finite code decodes and re-encodes to itself,
   midpoints round to the even code, saturation, torch's float8_e4m3fn cast
   on the finite range, brute-force nearest code).
@@ -66,6 +68,7 @@ def _load():
         lib = ctypes.CDLL(build())
         lib.oracle_round_bf16.argtypes = [_P, _P, _I]
         lib.oracle_fp8_e4m3.argtypes = [_P, _P, _I]
+        lib.oracle_gated_residual_transposed.argtypes = [_P, _P, _P, _I, _P, _I, _I, _I]
         lib.oracle_gated_ln_modulate.argtypes = [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F,
                                                  _P]
         lib.oracle_ln_modulate_fp8.argtypes = [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F]
@@ -268,3 +271,18 @@ def gated_ln_modulate(r, h, gate, scale, shift, eps, with_stats=False):
     _load().oracle_gated_ln_modulate(_ptr(r), _ptr(h), _ptr(g), _ptr(sc), _ptr(sh), vs,
                                      _ptr(r_out), _ptr(y), B, T, D, float(eps), _ptr(st))
     return (r_out, y, st) if with_stats else (r_out, y)
+
+
+def gated_residual_transposed(r, h, gate):
+    """r, h: the residual [B, D, T] and the update [B, T, D] (bf16 bits);
+    gate [B, D].  Returns r' = bf16(r + bf16(gate * h^T)) as [B, D, T]."""
+    r = _rows(r, "r")
+    h = _rows(h, "h")
+    B, D, T = r.shape
+    if h.shape != (B, T, D):
+        raise ValueError("h must be [B, T, D] for a residual [B, D, T]")
+    g, gs = _vec(gate, B, D, "gate")
+    vs = _vec_stride([(g, gs)])
+    out = np.empty_like(r)
+    _load().oracle_gated_residual_transposed(_ptr(r), _ptr(h), _ptr(g), vs, _ptr(out), B, T, D)
+    return out

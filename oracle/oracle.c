@@ -421,6 +421,30 @@ void oracle_qk_norm_rope_epilogue(const bf16_bits *q_txt, const bf16_bits *k_txt
                         rope_img, eps_txt, eps_img, q_out, k_out, v_out, rstd_out);
 }
 
+/* ------------------------------------- residual gating, transposed layout */
+
+/* The residual stream in the [B, hidden, tokens] layout: r, r_out are
+ * [B, D, T], the update h is [B, T, D] (logical row-major), gate [B, D]
+ * with batch stride vs:  r_out[b,d,t] = bf(rn(r[b,d,t] + bf(rn(gate[b,d] *
+ * h[b,t,d])))).  The guide's residual-gating variant ("Norm variants /
+ * residual gating"): the transposed dense path reads the update in logical
+ * row-major order and keeps the residual reads and output writes in their
+ * [B, hidden, tokens] layout. */
+void oracle_gated_residual_transposed(const bf16_bits *r, const bf16_bits *h,
+                                      const bf16_bits *gate, int64_t vs, bf16_bits *r_out,
+                                      int64_t B, int64_t T, int64_t D)
+{
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t d = 0; d < D; ++d) {
+            const float g = widen(gate[b * vs + d]);
+            for (int64_t t = 0; t < T; ++t) {
+                const int64_t i = (b * D + d) * T + t;
+                const float gh = bf(rn_mul(g, widen(h[(b * T + t) * D + d])));
+                r_out[i] = narrow(rn_add(widen(r[i]), gh));
+            }
+        }
+}
+
 /* ------------------------------------------- LayerNorm + modulate + FP8 */
 
 /* fp32 -> FP8 E4M3 (OCP "e4m3fn": 1 sign, 4 exponent bits with bias 7, 3

@@ -692,3 +692,23 @@ def test_qk_variants_fp64_brute_force(orc, hd, neox):
             o = widen(out[row0:row0 + T]).astype(np.float64)
             o0, o1 = (o[..., :h], o[..., h:]) if neox else (o[..., 0::2], o[..., 1::2])
             assert np.all(np.abs(o0 - e0) <= tol) and np.all(np.abs(o1 - e1) <= tol)
+
+
+# ---------------------------------- residual gating in the transposed layout
+
+def test_gated_residual_transposed_against_torch(orc):
+    B, D, T = 2, 72, 37
+    r = synth.normal_bf16((B, D, T), 80)
+    h = synth.normal_bf16((B, T, D), 81)
+    gate = synth.normal_bf16((B, D), 82, 0.5)
+    got = orc.gated_residual_transposed(r, h, gate)
+    tr = torch.from_numpy(widen(r)).to(torch.bfloat16)
+    th = torch.from_numpy(widen(h)).to(torch.bfloat16).transpose(1, 2)   # logical [B, D, T]
+    tg = torch.from_numpy(widen(gate)).to(torch.bfloat16)[:, :, None]
+    want = (tr + tg * th).float().numpy()
+    assert np.array_equal(widen(got), want)
+    zero = orc.gated_residual_transposed(r, h, vec(B, D, 0.0))
+    assert np.array_equal(zero, r)
+    one = orc.gated_residual_transposed(r, h, vec(B, D, 1.0))
+    exact = widen(r).astype(np.float64) + np.swapaxes(widen(h), 1, 2).astype(np.float64)
+    assert np.array_equal(widen(one), bf16_of_f64(exact).astype(np.float32))
