@@ -650,6 +650,7 @@ CONFIGS = [
     ("N3 qk neox 256+4096 tokens x 24 heads x 128", "qk", 1, 0, 128, True),
     ("N3 qk 256+4096 tokens x 48 heads x 64", "qk", 1, 0, 64, False),
     ("N3 qk neox 256+4096 tokens x 48 heads x 64", "qk", 1, 0, 64, True),
+    ("N2 gated residual, [1,3072,4096] residual layout", "resid_t", 1, 4096, 3072, False),
 ]
 
 
@@ -658,8 +659,8 @@ def config_bytes(kind, B, T, D, weight):
     if kind == "qk":  # D is head_dim; 24 heads of 128 or 48 of 64
         heads, tok = 24 * 128 // D, T_TXT + T_IMG
         return 2 * tok * 3 * heads * D * 2 + 4 * D * 2 + tok * D * 4, tok
-    rows, nvec = B * T, {"rms": 2, "ln": 2, "gated": 3, "lnfp8": 2, "gatedln": 3}[kind]
-    io = {"rms": 4, "ln": 4, "gated": 8, "lnfp8": 3, "gatedln": 8}[kind]  # bytes per element
+    rows, nvec = B * T, {"rms": 2, "ln": 2, "gated": 3, "lnfp8": 2, "gatedln": 3, "resid_t": 1}[kind]
+    io = {"rms": 4, "ln": 4, "gated": 8, "lnfp8": 3, "gatedln": 8, "resid_t": 6}[kind]
     return io * rows * D + nvec * B * D * 2 + (D * 2 if weight else 0), rows
 
 
@@ -694,6 +695,9 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
                 ydt = torch.uint8 if kind == "lnfp8" else torch.bfloat16
                 st = dict(x=rnd(B, T, D), emb=emb, y=torch.empty(B, T, D, dtype=ydt, device=dev),
                           w=(1.0 + rnd(D, std=0.05).float()).to(torch.bfloat16) if weight else None)
+                if kind == "resid_t":  # residual [B, D, T], update [B, T, D]
+                    st = dict(x=rnd(B, D, T), h=rnd(B, T, D), emb=emb,
+                              y=torch.empty(B, D, T, dtype=torch.bfloat16, device=dev))
                 if kind in ("gated", "gatedln"):
                     st.update(h=rnd(B, T, D), r_out=torch.empty(B, T, D, dtype=torch.bfloat16, device=dev))
                 sets.append(st)
@@ -718,6 +722,8 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
                 ops.ln_modulate(st["x"], vec(0), vec(1), EPS, out=st["y"])
             elif kind == "lnfp8":
                 ops.ln_modulate_fp8(st["x"], vec(0), vec(1), 0.05, EPS, out=st["y"])
+            elif kind == "resid_t":
+                ops.gated_residual_transposed(st["x"], st["h"], vec(2), out=st["y"])
             elif kind == "gatedln":
                 ops.gated_ln_modulate(st["x"], st["h"], vec(0), vec(1), vec(2), EPS,
                                       r_out=st["r_out"], out=st["y"])

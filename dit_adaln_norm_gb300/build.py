@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdan.so")
 SOURCES = ["dan_rows_rms.cu", "dan_rows_gated.cu", "dan_rows_ln.cu", "dan_rows_lnfp8.cu",
-           "dan_rows_gatedln.cu", "dan_qk.cu", "dan_abi.cu", "dan_noalloc.cu"]
+           "dan_rows_gatedln.cu", "dan_qk.cu", "dan_resid_t.cu", "dan_abi.cu", "dan_noalloc.cu"]
 HEADERS = ["dan_device.cuh", "dan_internal.h", "dan_ring.cuh", "dan_rows.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

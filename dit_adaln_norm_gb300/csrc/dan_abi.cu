@@ -159,6 +159,24 @@ int validate_gated_ln(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate
     return check_buffers(ins, 5, outs, 2, inplace, 1);
 }
 
+int validate_resid_t(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate, int64_t vs,
+                     const dan_bf16 *r_out, int64_t B, int64_t T, int64_t D, bool *empty)
+{
+    if (B < 0 || T < 0 || D < 0) return DAN_EINVAL;
+    if (D % 8 || D < 8) return DAN_EUNSUPPORTED;
+    if (B > 0 && T > kMaxElems / B) return DAN_EINVAL;
+    if (B * T > kMaxElems / D) return DAN_EINVAL;
+    *empty = (B * T == 0);
+    if (*empty) return DAN_OK;
+    if (vs < D || vs > kMaxElems || (B - 1) > kMaxElems / vs) return DAN_EINVAL;
+    if (vs % 8) return DAN_EALIGN;
+    const int64_t bytes = B * T * D * 2;
+    Buf ins[3] = {{r, span(r, bytes)}, {h, span(h, bytes)}, {gate, span(gate, vec_bytes(B, D, vs))}};
+    Buf outs[1] = {{r_out, span(r_out, bytes)}};
+    const int inplace[1][2] = {{0, 0}}; // r_out == r
+    return check_buffers(ins, 3, outs, 1, inplace, 1);
+}
+
 int validate_ln_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift, int64_t vs,
                     float qscale, const uint8_t *q, int64_t B, int64_t T, int64_t D, float eps,
                     bool *empty)
@@ -454,6 +472,25 @@ int dan_gated_ln_modulate(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *
     if (st != DAN_OK || empty) return st;
     dan::RowProblem p{r, h, gate, nullptr, scale, shift, vec_bstride, y, r_out, B, T, D, eps};
     return launched(dan::launch_gated_ln_modulate(p, static_cast<cudaStream_t>(stream)));
+}
+
+int dan_can_use_gated_residual_transposed(const dan_bf16 *r, const dan_bf16 *h,
+                                          const dan_bf16 *gate, int64_t vec_bstride,
+                                          const dan_bf16 *r_out, int64_t B, int64_t T, int64_t D)
+{
+    bool empty;
+    return validate_resid_t(r, h, gate, vec_bstride, r_out, B, T, D, &empty);
+}
+
+int dan_gated_residual_transposed(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate,
+                                  int64_t vec_bstride, dan_bf16 *r_out, int64_t B, int64_t T,
+                                  int64_t D, void *stream)
+{
+    bool empty;
+    const int st = validate_resid_t(r, h, gate, vec_bstride, r_out, B, T, D, &empty);
+    if (st != DAN_OK || empty) return st;
+    const dan::ResidProblem p{r, h, gate, r_out, B, T, D, vec_bstride};
+    return launched(dan::launch_gated_residual_transposed(p, static_cast<cudaStream_t>(stream)));
 }
 
 int dan_can_use_ln_modulate_fp8(const dan_bf16 *x, const dan_bf16 *scale, const dan_bf16 *shift,

@@ -58,6 +58,16 @@ cudaError_t launch_overlapped(void (*fn)(KArgs...), int grid, int block, int sme
     return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
+// Residual gating in the [B, hidden, tokens] layout: r, r_out [B, D, T],
+// h [B, T, D], gate [B, D] with batch stride vs.  Validated by the shim.
+struct ResidProblem {
+    const void *r, *h, *gate;
+    void *r_out;
+    int64_t B, T, D, vs;
+};
+
+cudaError_t launch_gated_residual_transposed(const ResidProblem &p, cudaStream_t s);
+
 cudaError_t launch_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_gated_rms_modulate(const RowProblem &p, cudaStream_t s);
 cudaError_t launch_ln_modulate(const RowProblem &p, cudaStream_t s);

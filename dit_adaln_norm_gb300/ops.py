@@ -34,6 +34,8 @@ _SIGS = {
     "dan_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F, _P],
     "dan_can_use_ln_modulate": [_P, _P, _P, _I, _P, _I, _I, _I, _F],
     "dan_ln_modulate_fp8": [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F, _P],
+    "dan_gated_residual_transposed": [_P, _P, _P, _I, _P, _I, _I, _I, _P],
+    "dan_can_use_gated_residual_transposed": [_P, _P, _P, _I, _P, _I, _I, _I],
     "dan_gated_ln_modulate": [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F, _P],
     "dan_can_use_gated_ln_modulate": [_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _F],
     "dan_can_use_ln_modulate_fp8": [_P, _P, _P, _I, _F, _P, _I, _I, _I, _F],
@@ -206,6 +208,27 @@ def gated_ln_modulate(r, h, gate, scale, shift, eps: float, r_out=None, out=None
                                         vs, _ptr(r_out), _ptr(y), B, T, D, float(eps),
                                         _stream()), "dan_gated_ln_modulate")
     return r_out, y
+
+
+def gated_residual_transposed(r, h, gate, out=None):
+    """r: the residual [B, D, T] (the [B, hidden, tokens] layout); h: the
+    update [B, T, D]; gate [B, D] (or [D] when B == 1).  Returns
+    r' = bf16(r + bf16(gate * h^T)) as [B, D, T]."""
+    _bf16_cuda(r, "r")
+    _bf16_cuda(h, "h")
+    if r.dim() != 3 or not r.is_contiguous():
+        raise ValueError("r: expected a contiguous [B, D, T] tensor")
+    B, D, T = r.shape
+    if tuple(h.shape) != (B, T, D) or not h.is_contiguous():
+        raise ValueError("h: expected a contiguous [B, T, D] tensor")
+    vs = _vectors(B, D, [("gate", gate)])
+    y = torch.empty_like(r) if out is None else out
+    _bf16_cuda(y, "out")
+    if tuple(y.shape) != (B, D, T) or not y.is_contiguous():
+        raise ValueError("out: expected a contiguous [B, D, T] tensor")
+    _check(load().dan_gated_residual_transposed(_ptr(r), _ptr(h), _ptr(gate), vs, _ptr(y), B, T,
+                                                D, _stream()), "dan_gated_residual_transposed")
+    return y
 
 
 def ln_modulate_fp8(x, scale, shift, qscale: float, eps: float, out=None):

@@ -1,11 +1,13 @@
 /*
  * dan.h -- C ABI of the GB300 (sm_103a) fused adaLN norm+modulate kernels.
  *
- * Seven operations, each a single kernel launch on the caller's stream:
+ * Eight operations, each a single kernel launch on the caller's stream:
  *
  *   dan_ln_modulate         y = bf16(LayerNorm(x) * (1 + scale) + shift)
  *   dan_ln_modulate_fp8     q = e4m3(y * rn(1/qscale)), y as dan_ln_modulate
  *   dan_gated_ln_modulate   r' = bf16(r + bf16(gate * h)); y = ln_modulate(r')
+ *   dan_gated_residual_transposed  r' = bf16(r + bf16(gate * h)) with the
+ *                           residual in the [B, hidden, tokens] layout
  *   dan_rms_modulate        y = bf16(RMSNorm(x) [* w] * (1 + scale) + shift)
  *   dan_gated_rms_modulate  r' = bf16(r + bf16(gate * h)); y = rms_modulate(r')
  *   dan_qk_norm_rope_epilogue  per-head RMSNorm + interleaved RoPE of Q and K,
@@ -191,6 +193,24 @@ int dan_can_use_gated_ln_modulate(const dan_bf16 *r, const dan_bf16 *h, const da
                                   const dan_bf16 *scale, const dan_bf16 *shift,
                                   int64_t vec_bstride, const dan_bf16 *r_out, const dan_bf16 *y,
                                   int64_t B, int64_t T, int64_t D, float eps);
+
+/* --------------------------------- residual gating, transposed layout
+ * "SGLang diffusion fused-op package guide", norm variants, residual
+ * gating: the residual stream r and the output r_out are [B, D, T] (the
+ * [B, hidden, tokens] layout), the update h is [B, T, D] (logical
+ * row-major), gate [B, D] with batch stride vec_bstride (a multiple of 8,
+ * >= D):
+ *   r_out[b, d, t] = bf16(rn(r[b, d, t] + bf16(rn(gate[b, d] * h[b, t, d]))))
+ * The update is read through shared-memory tiles; the residual reads and
+ * r_out writes stay coalesced along the tokens (no transposed copy).
+ * Supported: D % 8 == 0, D >= 8, any T.  In place: r_out == r is allowed;
+ * r_out may not overlap h or gate.  All pointers 16-byte aligned. */
+int dan_gated_residual_transposed(const dan_bf16 *r, const dan_bf16 *h, const dan_bf16 *gate,
+                                  int64_t vec_bstride, dan_bf16 *r_out, int64_t B, int64_t T,
+                                  int64_t D, void *stream);
+int dan_can_use_gated_residual_transposed(const dan_bf16 *r, const dan_bf16 *h,
+                                          const dan_bf16 *gate, int64_t vec_bstride,
+                                          const dan_bf16 *r_out, int64_t B, int64_t T, int64_t D);
 
 /* ------------------------------------------- LayerNorm + modulate + FP8
  * "SGLang diffusion fused-op package guide", list of fused producers:

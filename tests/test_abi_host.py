@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = ops.declared_symbols()
-    assert len(names) == 18
+    assert len(names) == 20
     for n in names:
         assert hasattr(lib, n), n
 
@@ -100,6 +100,17 @@ def test_gated_ln_validation(lib):
     assert f(ro=R) == OK               # residual updated in place
     assert f(y=R) == EALIAS and f(ro=H) == EALIAS and f(y=RO) == EALIAS
     assert f(D=12, vs=16) == EUNSUP and f(g=None) == EINVAL and f(h=G + 8) == EALIGN
+
+
+def test_gated_residual_transposed_validation(lib):
+    def f(r=R, h=H, g=G, vs=3072, ro=RO, B=1, T=4096, D=3072):
+        return lib.dan_can_use_gated_residual_transposed(r, h, g, vs, ro, B, T, D)
+
+    assert f() == OK and f(T=4093) == OK and f(ro=R) == OK
+    assert f(D=12, vs=16) == EUNSUP and f(D=0, vs=8) == EUNSUP
+    assert f(ro=H) == EALIAS and f(ro=R + 64) == EALIAS
+    assert f(h=H + 8) == EALIGN and f(B=2, vs=3076) == EALIGN and f(B=2, vs=3000) == EINVAL
+    assert f(g=None) == EINVAL and f(T=0, r=None, h=None, ro=None) == OK
 
 
 def test_ln_fp8_validation(lib):

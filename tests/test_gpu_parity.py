@@ -400,3 +400,35 @@ def test_gated_ln_in_place_and_shapes():
     run_gated_ln(1, 97, 3072, 510, inplace=True)
     run_gated_ln(1, 4216, 4096, synth.SEED_X)
     run_gated_ln(2, 1140, 4096, synth.SEED_X + 2)
+
+
+# ---------------------------------- residual gating in the transposed layout
+
+def run_resid_t(B, D, T, seed, inplace=False):
+    r = synth.normal_bf16((B, D, T), seed)
+    h = synth.normal_bf16((B, T, D), seed + 1)
+    emb = synth.normal_bf16((B, 6 * D), seed + 2, 0.5)
+    g = emb[:, 2 * D:3 * D]
+    dg = to_dev(emb)[:, 2 * D:3 * D]
+    dr = to_dev(r)
+    if inplace:
+        out = dr
+    else:
+        buf, out = guarded((B, D, T))
+    ops.gated_residual_transposed(dr, to_dev(h), dg, out=out)
+    torch.cuda.synchronize()
+    if not inplace:
+        check_guard(buf)
+    assert_bits_equal(from_dev(out), oracle.gated_residual_transposed(r, h, g),
+                      f"resid_t B={B} D={D} T={T}")
+
+
+@pytest.mark.parametrize("B,D,T", [(1, 8, 1), (1, 72, 37), (2, 64, 64), (1, 136, 130),
+                                   (2, 3072, 97), (1, 256, 4093)])
+def test_gated_residual_transposed_shapes(B, D, T):
+    run_resid_t(B, D, T, 700 + D + T)
+
+
+def test_gated_residual_transposed_in_place_and_site():
+    run_resid_t(1, 3072, 4096, 710, inplace=True)
+    run_resid_t(2, 3072, 512, 711)
