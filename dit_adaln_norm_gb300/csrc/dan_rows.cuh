@@ -1,21 +1,23 @@
 // dan_rows.cuh -- fused norm + adaLN modulate row kernels for sm_103a
-// (included by dan_rows_rms.cu, dan_rows_gated.cu and dan_rows_ln.cu,
-// which instantiate and launch them).
+// (included by dan_rows_rms.cu, dan_rows_gated.cu, dan_rows_ln.cu,
+// dan_rows_lnfp8.cu, dan_rows_gatedln.cu and dan_noalloc.cu, which
+// instantiate and launch them).
 //
 // RMSNorm ("SGLang diffusion fused-op package guide", section "Norm +
 // scale/shift (adaLN)"; "PR #33854 report", key source excerpt) and
 // LayerNorm without affine by Welford ("PR #34126 report", motivation
 // section), each followed by the aten modulate chain
-// y = bf16(bf16(n * bf16(1 + scale)) + shift).  The gated form first
-// forms r' = bf16(r + bf16(gate * h)) and stores it.
+// y = bf16(bf16(n * bf16(1 + scale)) + shift).  The gated forms first
+// form r' = bf16(r + bf16(gate * h)) and store it; the FP8 form quantises
+// y to E4M3 with a static scale.
 //
 // Design (HBM-bound row work, no tensor cores):
-//  - One CTA per SM takes a contiguous block of rows.  Its producer thread
-//    streams the rows into a ring of shared-memory slots with TMA bulk
-//    copies (cp.async.bulk, completion counted on mbarriers, see
-//    dan_ring.cuh), in row order, about eight rows ahead; consumer warps
-//    take one row each, copy it from the slot into registers, release the
-//    slot and compute while later rows are in flight.  Each row is read
+//  - One CTA per SM takes a contiguous block of rows.  Its warps form teams
+//    (one to four warps per row); each team requests its own rows with
+//    bulk copies (cp.async.bulk, completion counted on mbarriers, see
+//    dan_ring.cuh) into its own shared-memory slots, one or two rows
+//    ahead, copies each row from its slot into registers, refills the slot
+//    and computes while the next rows are in flight.  Each row is read
 //    from HBM once.
 //  - The arithmetic of a row depends only on the row's columns, never on
 //    which warp, CTA or launch computes it, so the output bits are
@@ -28,10 +30,10 @@
 //  - Canonical RMS order: logical thread tx (TPR = D/64 of them) owns the
 //    fragments TPR*b + tx (b = 0..7) as one sequential chain; lanes fold by
 //    the butterfly (= the adjacent-pair tree); logical warp sums fold by the
-//    adjacent-pair tree padded with +0.  A consumer warp carries all D/2048
+//    adjacent-pair tree padded with +0.  A team's warps share the D/2048
 //    logical warps of its row.
-//  - LayerNorm: 128 logical threads (four logical warps in one consumer
-//    warp), thread t owns fragments t + 128k; Welford per element with
+//  - LayerNorm: 128 logical threads (four logical warps, shared by the
+//    team's warps), thread t owns fragments t + 128k; Welford per element with
 //    rn(1/n) from a host-computed table; equal-count rows fold in shfl.down
 //    order with c = 1/2, ragged rows with the general combine through an
 //    ordered xor butterfly; the four warp states fold as (W0 + W2) + (W1 + W3).

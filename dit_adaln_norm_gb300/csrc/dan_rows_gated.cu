@@ -1,4 +1,4 @@
-// dan_rows_gated.cu -- launches of the gated-residual RMSNorm + modulate ring
+// dan_rows_gated.cu -- launches of the gated-residual RMSNorm + modulate row
 // kernel.
 #include "dan_rows.cuh"
 

@@ -1,4 +1,4 @@
-// dan_rows_ln.cu -- launches of the LayerNorm + modulate ring kernel, and
+// dan_rows_ln.cu -- launches of the LayerNorm + modulate row kernel, and
 // the bounded-wait self-test kernel.
 #include "dan_rows.cuh"
 
@@ -7,7 +7,7 @@ namespace dan {
 // ------------------------------------------------- bounded-wait self-test
 
 // One warp waits on an mbarrier that nothing completes, through the same
-// bounded wait the ring kernels use, and records the timeout.
+// bounded wait the row kernels use, and records the timeout.
 __global__ void wait_selftest_kernel(unsigned *status, unsigned long long limit_ns)
 {
     __shared__ uint64_t bar;

@@ -1,12 +1,14 @@
-// dan_rows_rms.cu -- launches of the RMSNorm + modulate ring kernel.
+// dan_rows_rms.cu -- launches of the RMSNorm + modulate row kernel.
 #include "dan_rows.cuh"
 
 namespace dan {
 
 // Pipeline shapes (warps NW, warps per row TW, slots per team SPC), chosen
-// by measurement: eight single-warp teams did better than fewer teams with
-// more slots each, or more warps (which cap the registers a row needs);
-// rows of 8192 are shared by four warps, which keeps them in registers.
+// by measurement: single-warp teams with two slots each, twelve of them
+// when there are many rows per SM and eight otherwise, did better than
+// fewer teams with more slots or multi-warp teams at these widths; rows of
+// 6144 and 8192 are shared by three and four warps, which keeps them in
+// registers.
 cudaError_t launch_rms_modulate(const RowProblem &q, cudaStream_t s)
 {
     switch (q.D) {

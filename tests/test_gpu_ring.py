@@ -1,10 +1,10 @@
-"""The bulk-copy ring under stress, and its bounded waits.
+"""The bulk-copy pipelines under stress, and their bounded waits.
 
-Every kernel streams rows through a shared-memory ring that each CTA
+Every kernel streams rows through shared-memory slots that each warp team
 refills many times at these sizes; repeated launches must all be bit-exact
-(a missing ordering between a consumer's reads and the next refill showed
-up as an occasional wrong row).  A wait that runs out must report through
-the device status word and leave the context usable."""
+(a missing ordering between a warp's reads of a slot and its next refill
+showed up as an occasional wrong row).  A wait that runs out must report
+through the device status word and leave the context usable."""
 import numpy as np
 import pytest
 import torch
