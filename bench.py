@@ -754,15 +754,25 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
     return out
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without comments and blank lines (string literals kept)."""
+    import re
+    pattern = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"', re.S)
+    out = pattern.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", src)
+    return "\n".join(line.rstrip() for line in out.splitlines() if line.strip())
+
+
 def kernel_sources_digest():
-    """sha256 over the CUDA sources, to tie stored counters to a kernel build."""
+    """sha256 over the CUDA sources with their comments removed, to tie
+    stored counters to the code they were taken on (a comment edit keeps
+    the digest; any code change voids it)."""
     import hashlib
     d = hashlib.sha256()
     csrc = os.path.join(ROOT, "dit_adaln_norm_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
             d.update(f.encode())
-            d.update(open(os.path.join(csrc, f), "rb").read())
+            d.update(_strip_comments(open(os.path.join(csrc, f)).read()).encode())
     return d.hexdigest()
 
 
