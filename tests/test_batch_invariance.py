@@ -115,3 +115,58 @@ def test_qk_token_subsets_match_joint_run():
         RI[c:d].contiguous(), EPS, EPS, H)]
     for g, f in zip(part, full):
         assert_bits_equal(g, np.concatenate([f[a:b], f[Tt + c:Tt + d]]), "qk token slices")
+
+
+def test_ln_fp8_batch_invariance(cfg_inputs):
+    x, sc, sh = cfg_inputs
+    qscale = 0.05
+    want = oracle.ln_modulate_fp8(x, sc, sh, qscale, EPS)
+    dsc, dsh = to_dev(np.ascontiguousarray(sc)), to_dev(np.ascontiguousarray(sh))
+    full = ops.ln_modulate_fp8(to_dev(x), dsc, dsh, qscale, EPS).cpu().numpy()
+    assert np.array_equal(full, want)
+    idx = np.repeat(np.arange(B), T)  # one launch of 2280 single-row batches
+    many = ops.ln_modulate_fp8(to_dev(x.reshape(B * T, 1, D)), dsc[idx], dsh[idx], qscale, EPS)
+    assert np.array_equal(many.cpu().numpy().reshape(B, T, D), want)
+    for b in range(B):
+        part = ops.ln_modulate_fp8(to_dev(x[b:b + 1, 40:700]), dsc[b:b + 1], dsh[b:b + 1],
+                                   qscale, EPS)
+        assert np.array_equal(part.cpu().numpy()[0], want[b, 40:700])
+
+
+def test_gated_ln_batch_invariance(cfg_inputs):
+    x, sc, sh = cfg_inputs
+    sc, sh = np.ascontiguousarray(sc), np.ascontiguousarray(sh)
+    h = synth.normal_bf16((B, T, D), 7)
+    gate = synth.normal_bf16((B, D), 8, 0.1)
+    want_r, want_y = oracle.gated_ln_modulate(x, h, gate, sc, sh, EPS)
+    dg, dsc, dsh = to_dev(gate), to_dev(sc), to_dev(sh)
+    r_all, y_all = ops.gated_ln_modulate(to_dev(x), to_dev(h), dg, dsc, dsh, EPS)
+    assert_bits_equal(from_dev(r_all), want_r, "gated ln r' full")
+    assert_bits_equal(from_dev(y_all), want_y, "gated ln y full")
+    idx = np.repeat(np.arange(B), T)
+    r_m, y_m = ops.gated_ln_modulate(to_dev(x.reshape(B * T, 1, D)), to_dev(h.reshape(B * T, 1, D)),
+                                     dg[idx], dsc[idx], dsh[idx], EPS)
+    assert_bits_equal(from_dev(r_m).reshape(B, T, D), want_r, "gated ln r' single rows")
+    assert_bits_equal(from_dev(y_m).reshape(B, T, D), want_y, "gated ln y single rows")
+
+
+@pytest.mark.parametrize("hd,neox", [(128, True), (64, False), (64, True)])
+def test_qk_variant_token_subsets(hd, neox):
+    H, Tt, Ti = 24 * 128 // hd, 64, 300
+    pt, pi = synth.packed_qkv(Tt, H, 93, hd), synth.packed_qkv(Ti, H, 94, hd)
+    ws = synth.head_weights(4, 95, hd)
+    rt, ri = synth.rope_table(Tt, hd), synth.rope_table(Ti, hd, pos0=Tt)
+    dw = [to_dev(w) for w in ws]
+    Pt, Pi = to_dev(pt), to_dev(pi)
+    RT, RI = torch.from_numpy(rt).cuda(), torch.from_numpy(ri).cuda()
+    run = lambda a, b, ra, rb: [from_dev(o) for o in ops.qk_norm_rope_epilogue(
+        synth.split_qkv(a, H, hd), synth.split_qkv(b, H, hd), *dw, ra, rb, EPS, EPS, H,
+        head_dim=hd, neox=neox)]
+    full = run(Pt, Pi, RT, RI)
+    want = oracle.qk_norm_rope_epilogue(synth.split_qkv(pt, H, hd), synth.split_qkv(pi, H, hd),
+                                        H, ws, rt, ri, EPS, EPS, head_dim=hd, neox=neox)
+    for g, w in zip(full, want):
+        assert_bits_equal(g, w, f"qk hd={hd} neox={neox} joint")
+    part = run(Pt[5:40], Pi[17:250], RT[5:40].contiguous(), RI[17:250].contiguous())
+    for g, f in zip(part, full):
+        assert_bits_equal(g, np.concatenate([f[5:40], f[Tt + 17:Tt + 250]]), "qk variant slices")
