@@ -664,12 +664,14 @@ def config_bytes(kind, B, T, D, weight):
     return io * rows * D + nvec * B * D * 2 + (D * 2 if weight else 0), rows
 
 
-def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
+def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20, eager_only=0):
     """Launch time of every configuration: a graph of launches cycling over
     enough buffer sets that ~2x L2 of other traffic separates two uses of a
     buffer (up to max_sets; smaller configurations stay L2-resident and say
     so).  Inputs are drawn on the device (normal, seeded): the kernels'
-    time does not depend on the values."""
+    time does not depend on the values.  eager_only = k > 0 instead runs
+    each configuration k times without graphs or timing (for an ncu
+    capture of every configuration's DRAM traffic) and returns None."""
     import torch
     from dit_adaln_norm_gb300 import ops
     from dit_adaln_norm_gb300.synth import split_qkv
@@ -733,6 +735,14 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
 
         reps = max(32, nsets)
         torch.cuda.synchronize()  # inputs were drawn on the default stream
+        if eager_only:
+            with torch.cuda.stream(stream):
+                for i in range(eager_only):
+                    launch(sets[i % nsets])
+            torch.cuda.synchronize()
+            del sets
+            torch.cuda.empty_cache()
+            continue
         with torch.cuda.stream(stream):
             for st in sets:
                 launch(st)
@@ -751,7 +761,7 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20):
                      "l2_resident": nsets * nbytes < min_bytes}
         del sets, graph
         torch.cuda.empty_cache()
-    return out
+    return None if eager_only else out
 
 
 def _strip_comments(src: str) -> str:
@@ -799,6 +809,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration kernel timings")
+    ap.add_argument("--config-launches", type=int, default=0,
+                    help="only launch every configuration this many times, untimed (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -812,6 +824,16 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         tdist.init_process_group("nccl")
         dist = tdist
+    if args.config_launches > 0:
+        import torch
+        from dit_adaln_norm_gb300 import build as dan_build
+        dan_build.build()
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        time_configs(dev, torch.cuda.Stream(device=dev), eager_only=args.config_launches)
+        print(json.dumps({"config_launches": args.config_launches,
+                          "configs": [c[0] for c in CONFIGS]}))
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:
