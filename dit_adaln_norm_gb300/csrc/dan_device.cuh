@@ -95,6 +95,16 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ uint4 ld_vec(const uint4 *p) { return __ldg(p); }
 __device__ __forceinline__ float4 ld_vec(const float4 *p) { return __ldg(p); }
 
+// rn(x / D) for a divisor D known at compile time.  For a power of two it
+// is the multiply by the exact reciprocal 2^-k: both give the exact
+// quotient rounded once, so the bits are those of the IEEE division.
+template <int D>
+__device__ __forceinline__ float div_by(float x)
+{
+    if constexpr ((D & (D - 1)) == 0) return __fmul_rn(x, 1.0f / (float)D);
+    else return __fdiv_rn(x, (float)D);
+}
+
 // The defined reciprocal square root: rn(1 / rn(sqrt(v))), two IEEE ops.
 __device__ __forceinline__ float defined_rsqrt(float v)
 {

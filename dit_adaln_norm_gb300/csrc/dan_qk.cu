@@ -217,7 +217,7 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
     float my_rstd[S::NK];
 #pragma unroll
     for (int j = 0; j < S::NK; ++j)
-        my_rstd[j] = defined_rsqrt(__fadd_rn(__fdiv_rn(ps[j], (float)HD), p.eps[U.s_]));
+        my_rstd[j] = defined_rsqrt(__fadd_rn(div_by<HD>(ps[j]), p.eps[U.s_]));
 
     float2 w2[4], cc[4], sn[4];
 #pragma unroll

@@ -63,6 +63,7 @@ struct RowParams {
     int Bs;      // batches staged in shared memory; 0 = read vectors from global
     int F;       // fragments per row (D / 8)
     float eps;
+    float inv_d; // 1 / D when D is a power of two (exact), else 0
     unsigned *status;            // device status word (bounded-wait failures)
     unsigned long long limit_ns; // bound of every wait
     unsigned *cta_status;        // per-CTA failure records (CTA_STATUS kernels only)
@@ -222,7 +223,7 @@ __device__ __forceinline__ float rms_rstd(const float (&sums)[LW], float eps)
     for (int off = 1; off < P2; off <<= 1)
 #pragma unroll
         for (int k = 0; k < P2; k += 2 * off) t[k] = __fadd_rn(t[k], t[k + off]);
-    return defined_rsqrt(__fadd_rn(__fdiv_rn(t[0], (float)D), eps));
+    return defined_rsqrt(__fadd_rn(div_by<D>(t[0]), eps));
 }
 
 // Modulate two rows of normalised fp32 values t[e] (one fragment) and store:
@@ -481,7 +482,10 @@ __device__ __forceinline__ void ln_store(const float (&x)[J][FPT][8], int r, flo
                                          const uint4 *s_vec, int lane)
 {
     const int F = p.F;
-    const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(__fdiv_rn(m2, (float)(8 * F)), p.eps)));
+    // rn(m2 / D): a multiply by the exact reciprocal when D is a power of
+    // two (the same bits as the division), else the IEEE division
+    const float var = p.inv_d != 0.0f ? __fmul_rn(m2, p.inv_d) : __fdiv_rn(m2, (float)(8 * F));
+    const float2 rstd2 = dup2(defined_rsqrt(__fadd_rn(var, p.eps)));
     const float2 mean2 = dup2(mean);
     uint4 *y = FP8 ? nullptr : p.y + row * F;
     uint2 *q8 = FP8 ? p.q8 + row * F : nullptr;
@@ -806,6 +810,7 @@ RowParams make_params(const RowProblem &q)
     p.vs8 = q.vs / 8;
     p.F = (int)(q.D / 8);
     p.eps = q.eps;
+    p.inv_d = (q.D & (q.D - 1)) == 0 ? 1.0f / (float)q.D : 0.0f;
     p.Bs = 0;
     p.status = device_status();
     p.limit_ns = kWaitLimitNs;
