@@ -8,13 +8,24 @@
 // .contiguous() copy of the residual).  Per element
 //   r_out[b, d, t] = bf16(rn(r[b, d, t] + bf16(rn(gate[b, d] * h[b, t, d])))).
 //
-// 64-token x 64-channel tiles: the update tile (64 token rows of 128
-// contiguous bytes) is read with 16-byte loads into shared memory with a
-// padded row pitch of 33 words, so that a warp reading one channel pair
-// across 32 tokens touches 32 different banks; each warp takes channel
-// pairs, each lane two neighbouring tokens of both channels (4-byte loads
-// and stores of the residual, 128 contiguous bytes per warp).  A CTA's
-// next tile is loaded into registers while the current one is computed.
+// T % 8 == 0 (every residual row 16-byte aligned): a persistent kernel,
+// six CTAs of 64 threads per SM, each taking a contiguous run of
+// 64-channel x 64-token tiles (tokens fastest, so a CTA streams along its
+// 64 residual rows; measured faster than interleaving the CTAs' tiles, or
+// than running channels fastest).  Both inputs of a tile are staged in
+// shared memory by 16-byte asynchronous copies, one tile ahead: the update
+// as 64 token rows of 128 bytes, its 16-byte chunks XOR-swizzled by the
+// row's token octet, the residual as 64 channel rows of 128 bytes.  Each
+// thread then takes one channel octet x one token octet: eight 16-byte
+// shared loads of the update (one per token; the swizzle puts the eight
+// lanes of a load phase on eight different bank groups), eight of the
+// residual (one per channel), and eight 16-byte stores of r_out, each
+// eight lanes covering 128 contiguous bytes of one residual row.  The
+// product bf16(gate * h) is formed on channel pairs, as the update holds
+// them, and regrouped into token pairs with byte permutes before the add.
+//
+// Other T: 64 x 64 tiles, one per CTA, element by element on the residual
+// (its rows are not 16-byte aligned).
 #include "dan_device.cuh"
 #include "dan_internal.h"
 #include "dan_ring.cuh"
@@ -23,9 +34,8 @@ namespace dan {
 
 namespace {
 
-constexpr int kTile = 64;   // tokens and channels per tile
-constexpr int kPitchW = 33; // shared-memory words per update row (32 of data)
-constexpr int kResidThreads = 256;
+constexpr int kTile = 64;          // channels and tokens per tile
+constexpr int kResidThreads = 128; // 16 channel quads x 8 token octets
 
 struct ResidParams {
     const uint16_t *r;
@@ -40,30 +50,17 @@ struct ResidParams {
 __device__ __forceinline__ uint32_t lows(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410); }
 __device__ __forceinline__ uint32_t highs(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
 
-// Per-thread offsets that do not change from tile to tile.
-struct ResidLane {
-    int64_t hoff[2]; // update chunk j: token row (c >> 3) * D/8 + chunk (c & 7), in uint4
-    int64_t roff[4]; // channel pair j: (2 * (warp + 8 j)) * T + 2 * lane, in elements
-    int ht[2], hc[2]; // update chunk j: token row and chunk within the tile
-};
-
-// Registers of one tile in flight: its coordinates and this thread's update
-// chunks and, for a full tile with even T, its residual words.
-struct ResidTile {
-    uint4 h[2];
-    uint32_t r0[4], r1[4];
-    int64_t b, d0, t0;
-    int64_t rbase; // element index of r[b][d0][t0]
-    bool full;     // the whole 64 x 64 tile lies inside the tensor
-};
-
 // Tile order: within a batch, bands of kBand token tiles; in a band, the
 // channel tiles, and in each channel tile the band's token tiles, so the
 // tiles in flight at once cover whole update rows and runs of each
-// residual row.  32-bit tile arithmetic.
+// residual row.
 constexpr unsigned kBand = 16;
 
-__device__ __forceinline__ void tile_coords(const ResidParams &p, unsigned tile, ResidTile &u)
+struct TileAt {
+    unsigned b, d0, t0;
+};
+
+__device__ __forceinline__ TileAt tile_at(const ResidParams &p, unsigned tile)
 {
     const unsigned per_b = p.tiles_d * p.tiles_t;
     const unsigned b = tile / per_b, rem = tile - b * per_b;
@@ -78,128 +75,179 @@ __device__ __forceinline__ void tile_coords(const ResidParams &p, unsigned tile,
         dt = r2 / w;
         tt = full * kBand + (r2 - dt * w);
     }
-    u.b = b;
-    u.d0 = (int64_t)dt * kTile;
-    u.t0 = (int64_t)tt * kTile;
-    u.rbase = (p.D * u.b + u.d0) * p.T + u.t0;
-    u.full = u.t0 + kTile <= p.T && u.d0 + kTile <= p.D;
+    return TileAt{b, dt * kTile, tt * kTile};
 }
 
-// Issue the loads of a tile: the update chunks always (D % 8 == 0, so a
-// chunk is wholly inside or outside its row), the residual words for a
-// full tile when T is even (rows 4-byte aligned).
-template <bool EVEN_T>
-__device__ __forceinline__ void tile_load(const ResidParams &p, const ResidLane &L, unsigned tile,
-                                          ResidTile &u)
+// One 64 x 64 tile per CTA, element by element on the residual (any T).
+__global__ void __launch_bounds__(kResidThreads) gated_residual_t_kernel(const ResidParams p)
 {
-    tile_coords(p, tile, u);
-    const uint4 *h = p.h + ((p.T * u.b + u.t0) * p.D + u.d0) / 8;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        if (u.full || (u.t0 + L.ht[j] < p.T && u.d0 + 8 * L.hc[j] < p.D))
-            u.h[j] = ld_stream(h + L.hoff[j]);
-        else
-            u.h[j] = make_uint4(0, 0, 0, 0);
-    }
-    if (EVEN_T && u.full) {
-        const uint16_t *r = p.r + u.rbase;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            u.r0[j] = *reinterpret_cast<const uint32_t *>(r + L.roff[j]);
-            u.r1[j] = *reinterpret_cast<const uint32_t *>(r + L.roff[j] + p.T);
-        }
-    }
-}
-
-// The gated residual of one tile (its update chunks, and residual words
-// when loaded, in u).
-template <bool EVEN_T>
-__device__ __forceinline__ void tile_compute(const ResidParams &p, const ResidLane &L,
-                                             const ResidTile &u, uint32_t *s_h, uint32_t *s_g,
-                                             int warp, int lane)
-{
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        uint32_t *dst = s_h + L.ht[j] * kPitchW + 4 * L.hc[j];
-        dst[0] = u.h[j].x;
-        dst[1] = u.h[j].y;
-        dst[2] = u.h[j].z;
-        dst[3] = u.h[j].w;
-    }
-    if (threadIdx.x < kTile / 2) {
-        const int64_t d = u.d0 + 2 * threadIdx.x;
-        s_g[threadIdx.x] =
-            d < p.D ? *reinterpret_cast<const uint32_t *>(p.gate + u.b * p.vs + d) : 0u;
-    }
-    __syncthreads();
-
-    const int t = 2 * lane; // this lane's tokens t0 + t, t0 + t + 1
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int pr = warp + 8 * j;
-        const uint32_t g2 = s_g[pr];
-        const uint32_t gd = __byte_perm(g2, 0, 0x1010), gd1 = __byte_perm(g2, 0, 0x3232);
-        const uint32_t ht = s_h[t * kPitchW + pr], ht1 = s_h[(t + 1) * kPitchW + pr];
-        const uint32_t hd = lows(ht, ht1), hd1 = highs(ht, ht1); // (tokens t, t+1) per channel
-        uint16_t *out = p.r_out + u.rbase + L.roff[j];
-        if (EVEN_T && u.full) {
-            *reinterpret_cast<uint32_t *>(out) = gated_word(u.r0[j], gd, hd);
-            *reinterpret_cast<uint32_t *>(out + p.T) = gated_word(u.r1[j], gd1, hd1);
-        } else if (u.d0 + 2 * pr < p.D && u.t0 + t < p.T) {
-            // an edge tile, or rows not 4-byte aligned: token by token
-            const uint16_t *in = p.r + u.rbase + L.roff[j];
-            const bool two = u.t0 + t + 1 < p.T;
-            const uint32_t r0 = in[0] | (two ? (uint32_t)in[1] << 16 : 0u);
-            const uint32_t r1 = in[p.T] | (two ? (uint32_t)in[p.T + 1] << 16 : 0u);
-            const uint32_t w0 = gated_word(r0, gd, hd), w1 = gated_word(r1, gd1, hd1);
-            out[0] = (uint16_t)w0;
-            out[p.T] = (uint16_t)w1;
-            if (two) {
-                out[1] = (uint16_t)(w0 >> 16);
-                out[p.T + 1] = (uint16_t)(w1 >> 16);
-            }
-        }
-    }
-    __syncthreads(); // the tile's shared memory is reused by the next tile
-}
-
-// EVEN_T: T is even, so every residual row starts 4-byte aligned and a
-// lane's token pair can move as one word.  Each CTA walks its tiles two at
-// a time, the next tile's loads issued before the current one is computed.
-template <bool EVEN_T>
-__global__ void __launch_bounds__(kResidThreads, 4) gated_residual_t_kernel(const ResidParams p)
-{
-    __shared__ uint32_t s_h[kTile * kPitchW]; // update tile: [token][channel pair]
-    __shared__ uint32_t s_g[kTile / 2];       // gate pairs
+    __shared__ __align__(16) uint2 s_h[kTile][kTile / 4]; // update tile: [token][channel quad]
 
     grid_dependency_wait(); // no global access above this line
     allow_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    ResidLane L;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int c = threadIdx.x + kResidThreads * j;
-        L.ht[j] = c >> 3;
-        L.hc[j] = c & 7;
-        L.hoff[j] = (int64_t)L.ht[j] * (p.D / 8) + L.hc[j];
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) L.roff[j] = (int64_t)(2 * (warp + 8 * j)) * p.T + 2 * lane;
+    const TileAt at = tile_at(p, blockIdx.x);
+    const int64_t T = p.T, D = p.D;
+    const int tid = threadIdx.x;
 
-    unsigned tile = blockIdx.x;
-    if (tile >= p.tiles) return;
-    ResidTile A, Bt;
-    tile_load<EVEN_T>(p, L, tile, A);
-    for (;;) {
-        const unsigned t1 = tile + gridDim.x, t2 = t1 + gridDim.x;
-        if (t1 < p.tiles) tile_load<EVEN_T>(p, L, t1, Bt);
-        tile_compute<EVEN_T>(p, L, A, s_h, s_g, warp, lane);
-        if (t1 >= p.tiles) break;
-        if (t2 < p.tiles) tile_load<EVEN_T>(p, L, t2, A);
-        tile_compute<EVEN_T>(p, L, Bt, s_h, s_g, warp, lane);
-        if (t2 >= p.tiles) break;
-        tile = t2;
+    // Update tile: 64 rows x 8 chunks of 16 bytes; chunks outside the
+    // tensor read as zero (their products are never stored).
+    {
+        const int ch = tid & 7;
+        const bool col_in = (int64_t)at.d0 + 8 * ch < D; // D % 8 == 0: whole chunk
+        const uint4 *h = p.h + (((int64_t)at.b * T + at.t0) * D + at.d0) / 8 + ch;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int row = (tid >> 3) + 16 * j;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (col_in && (int64_t)at.t0 + row < T) v = ld_stream(h + (int64_t)row * (D / 8));
+            reinterpret_cast<uint4 *>(&s_h[row][0])[ch] = v;
+        }
     }
+    __syncthreads();
+
+    const int cq = tid & 15, tg = tid >> 4;   // channels 4cq..4cq+3, tokens 8tg..8tg+7
+    const int64_t d = (int64_t)at.d0 + 4 * cq; // D % 4 == 0: whole quad in or out
+    const int64_t t = (int64_t)at.t0 + 8 * tg;
+    if (d >= D || t >= T) return;
+    const int64_t rrow = ((int64_t)at.b * D + d) * T + t; // element index of r[b][d][t]
+    const uint2 g = *reinterpret_cast<const uint2 *>(p.gate + (int64_t)at.b * p.vs + d);
+    // gh on channel pairs: gh[k] = (channels 4cq, 4cq+1), gh[8+k] = (4cq+2, 4cq+3) of token t+k
+    uint32_t gh[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint2 hv = s_h[8 * tg + k][cq];
+        gh[k] = hmul2(g.x, hv.x);
+        gh[8 + k] = hmul2(g.y, hv.y);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // channel c, tokens (2q, 2q+1): low (c even) or high halves
+            const uint32_t a = gh[8 * (c >> 1) + 2 * q], b = gh[8 * (c >> 1) + 2 * q + 1];
+            const uint32_t ghw = (c & 1) ? highs(a, b) : lows(a, b);
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                if (t + 2 * q + e < T) {
+                    const int64_t i = rrow + c * T + 2 * q + e;
+                    const uint32_t w = hadd2((uint32_t)p.r[i], e ? ghw >> 16 : ghw & 0xFFFFu);
+                    p.r_out[i] = (uint16_t)w;
+                }
+        }
+}
+
+// ------------------------------------------------ the pipelined kernel
+
+constexpr int kPD = 64;         // channels per tile
+constexpr int kPT = 64;        // tokens per tile
+constexpr int kRC = kPT / 8;    // token octets per tile (16-byte chunks per residual row)
+constexpr int kHC = kPD / 8;    // channel octets per tile (16-byte chunks per update row)
+constexpr int kPThreads = kHC * kRC; // one thread per channel octet x token octet
+constexpr int kPipeCtas = 6;    // CTAs per SM (shared memory allows six)
+constexpr int kStages = 2;      // tiles in shared memory (kStages - 1 in flight)
+constexpr int kStageH = kPT * kPD / 8;  // 16-byte chunks of the update per tile
+constexpr int kStageR = kPD * kPT / 8;  // 16-byte chunks of the residual per tile
+
+struct PipeTile {
+    unsigned b, d0, t0;
+};
+
+// Tile i of the (batch, channel tile, token tile) order, tokens fastest.
+__device__ __forceinline__ PipeTile pipe_tile(const ResidParams &p, unsigned i)
+{
+    const unsigned tt = i % p.tiles_t, rest = i / p.tiles_t;
+    const unsigned dt = rest % p.tiles_d, b = rest / p.tiles_d;
+    return PipeTile{b, dt * kPD, tt * kPT};
+}
+
+// Issue this thread's asynchronous copies of tile i into stage buffers
+// (sh, sr).  Chunks outside the tensor are not copied: the outputs that
+// would read them are never stored.
+__device__ __forceinline__ void pipe_issue(const ResidParams &p, unsigned i, uint4 *sh, uint4 *sr)
+{
+    const PipeTile at = pipe_tile(p, i);
+    const int tid = threadIdx.x;
+    const int64_t T = p.T, D = p.D;
+    {   // update: kPT token rows x kHC chunks; chunk c of row k goes to slot c ^ ((k >> 3) & 7)
+        const int c = tid % kHC;
+        if ((int64_t)at.d0 + 8 * c < D) {
+            const uint4 *src = p.h + (((int64_t)at.b * T + at.t0) * D + at.d0) / 8 + c;
+#pragma unroll
+            for (int j = 0; j < kStageH / kPThreads; ++j) {
+                const int k = tid / kHC + (kPThreads / kHC) * j;
+                if ((int64_t)at.t0 + k < T)
+                    cp_async16(sh + k * kHC + (c ^ ((k >> 3) & 7)), src + (int64_t)k * (D / 8));
+            }
+        }
+    }
+    {   // residual: 64 channel rows x kRC chunks
+        const int u = tid % kRC;
+        if ((int64_t)at.t0 + 8 * u < T) {
+            const uint16_t *src = p.r + ((int64_t)at.b * D + at.d0) * T + at.t0 + 8 * u;
+#pragma unroll
+            for (int j = 0; j < kStageR / kPThreads; ++j) {
+                const int k = tid / kRC + (kPThreads / kRC) * j;
+                if ((int64_t)at.d0 + k < D) cp_async16(sr + k * kRC + u, src + (int64_t)k * T);
+            }
+        }
+    }
+}
+
+// CTA c takes tiles [c*N/G, (c+1)*N/G).  Requires T % 8 == 0.
+__global__ void __launch_bounds__(kPThreads, kPipeCtas) gated_residual_t_pipe_kernel(const ResidParams p)
+{
+    extern __shared__ __align__(128) uint4 s_pipe[]; // kStages x (update, residual)
+    grid_dependency_wait(); // no global access above this line
+    allow_dependents();
+    const unsigned G = gridDim.x;
+    const unsigned first = (unsigned)((uint64_t)blockIdx.x * p.tiles / G);
+    const unsigned n = (unsigned)((uint64_t)(blockIdx.x + 1) * p.tiles / G) - first;
+    auto tile_of = [&](unsigned i) { return first + i; };
+    auto stage_h = [&](unsigned i) { return s_pipe + (i % kStages) * (kStageH + kStageR); };
+    auto stage_r = [&](unsigned i) { return stage_h(i) + kStageH; };
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if ((unsigned)s < n) pipe_issue(p, tile_of(s), stage_h(s), stage_r(s));
+        cp_async_commit(); // one group per tile, empty past the end
+    }
+    const int o = threadIdx.x / kRC; // channel octet of the tile
+    const int v = threadIdx.x % kRC; // token octet of the tile
+    const int64_t T = p.T, D = p.D;
+    for (unsigned i = 0; i < n; ++i) {
+        cp_async_wait<kStages - 2>(); // this thread's copies of tile i have landed
+        __syncthreads();              // everyone's have; everyone is done with tile i - 1
+        if (i + kStages - 1 < n)
+            pipe_issue(p, tile_of(i + kStages - 1), stage_h(i + kStages - 1), stage_r(i + kStages - 1));
+        cp_async_commit();
+
+        const PipeTile at = pipe_tile(p, tile_of(i));
+        const int64_t d = (int64_t)at.d0 + 8 * o, t = (int64_t)at.t0 + 8 * v;
+        if (d >= D || t >= T) continue; // D, T multiples of 8: whole octets in or out
+        const uint4 g = *reinterpret_cast<const uint4 *>(p.gate + (int64_t)at.b * p.vs + d);
+        const uint4 *sh = stage_h(i), *sr = stage_r(i);
+        // gh[k]: channel pairs of token t + k, bf16(gate * h)
+        uint4 gh[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 hv = sh[(8 * v + k) * kHC + (o ^ (v & 7))];
+            gh[k] = make_uint4(hmul2(g.x, hv.x), hmul2(g.y, hv.y), hmul2(g.z, hv.z), hmul2(g.w, hv.w));
+        }
+        uint16_t *out = p.r_out + ((int64_t)at.b * D + d) * T + t;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 rv = sr[(8 * o + c) * kRC + v];
+            // channel c, token pair (2q, 2q+1): low (c even) or high halves
+            // of channel pair c / 2 in the two tokens' products
+            auto pair = [&](int q) -> uint32_t {
+                const uint32_t a = word(gh[2 * q], c >> 1), b = word(gh[2 * q + 1], c >> 1);
+                return (c & 1) ? highs(a, b) : lows(a, b);
+            };
+            const uint4 res = make_uint4(hadd2(rv.x, pair(0)), hadd2(rv.y, pair(1)),
+                                         hadd2(rv.z, pair(2)), hadd2(rv.w, pair(3)));
+            st_stream(reinterpret_cast<uint4 *>(out + (int64_t)c * T), res);
+        }
+    }
+    cp_async_wait_all(); // no copy outlives the CTA
 }
 
 } // namespace
@@ -219,11 +267,19 @@ cudaError_t launch_gated_residual_transposed(const ResidProblem &q, cudaStream_t
     p.tiles_t = (unsigned)tt;
     p.tiles_d = (unsigned)td;
     p.tiles = (unsigned)(q.B * tt * td);
-    const unsigned cap = (unsigned)sm_count() * 4; // 4 resident CTAs of 256 threads per SM
-    const int grid = (int)(p.tiles < cap ? p.tiles : cap);
-    if (q.T % 2 == 0)
-        return launch_overlapped(gated_residual_t_kernel<true>, grid, kResidThreads, 0, s, p);
-    return launch_overlapped(gated_residual_t_kernel<false>, grid, kResidThreads, 0, s, p);
+    if (q.T % 8 == 0) {
+        const int64_t ptiles = q.B * ((q.D + kPD - 1) / kPD) * ((q.T + kPT - 1) / kPT);
+        p.tiles_t = (unsigned)((q.T + kPT - 1) / kPT);
+        p.tiles_d = (unsigned)((q.D + kPD - 1) / kPD);
+        p.tiles = (unsigned)ptiles; // at most the 64 x 64 tile count checked above
+        constexpr int smem = kStages * (kStageH + kStageR) * 16;
+        const cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void *>(gated_residual_t_pipe_kernel), smem);
+        if (e != cudaSuccess) return e;
+        const int64_t cap = (int64_t)sm_count() * kPipeCtas;
+        const int grid = (int)(ptiles < cap ? ptiles : cap);
+        return launch_overlapped(gated_residual_t_pipe_kernel, grid, kPThreads, smem, s, p);
+    }
+    return launch_overlapped(gated_residual_t_kernel, (int)p.tiles, kResidThreads, 0, s, p);
 }
 
 } // namespace dan

@@ -424,7 +424,8 @@ def run_resid_t(B, D, T, seed, inplace=False):
 
 
 @pytest.mark.parametrize("B,D,T", [(1, 8, 1), (1, 72, 37), (2, 64, 64), (1, 136, 130),
-                                   (2, 3072, 97), (1, 256, 4093)])
+                                   (2, 3072, 97), (1, 256, 4093), (1, 8, 8), (1, 72, 136),
+                                   (2, 200, 8), (3, 520, 72)])
 def test_gated_residual_transposed_shapes(B, D, T):
     run_resid_t(B, D, T, 700 + D + T)
 
