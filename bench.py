@@ -811,9 +811,13 @@ def main():
                     help="skip the per-configuration kernel timings")
     ap.add_argument("--config-launches", type=int, default=0,
                     help="only launch every configuration this many times, untimed (for ncu)")
+    ap.add_argument("--config-filter", default="",
+                    help="keep only the configurations whose name contains this text")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.config_filter:
+        CONFIGS[:] = [c for c in CONFIGS if args.config_filter in c[0]]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
