@@ -58,7 +58,7 @@ extern "C" int dan_rms_modulate_noalloc(const dan_bf16 *x, const dan_bf16 *weigh
         e = dan::many_rows(q) ? dan::launch_ring<dan::kRms, 2, 8, 12, 1, 2, false, true>(q, s, scratch)
                               : dan::launch_ring<dan::kRms, 2, 8, 8, 1, 2, false, true>(q, s, scratch);
         break;
-    case 6144: e = dan::launch_ring<dan::kRms, 3, 8, 12, 3, 1, false, true>(q, s, scratch); break;
+    case 6144: e = dan::launch_ring<dan::kRms, 3, 8, 12, 3, 2, false, true>(q, s, scratch); break;
     default: e = dan::launch_ring<dan::kRms, 4, 8, 16, 4, 1, false, true>(q, s, scratch); break;
     }
     return e == cudaSuccess ? DAN_OK : DAN_ECUDA;

@@ -15,7 +15,7 @@ cudaError_t launch_rms_modulate(const RowProblem &q, cudaStream_t s)
     case 2048: return launch_ring<kRms, 1, 8, 8, 1, 2, false>(q, s);
     case 4096: return many_rows(q) ? launch_ring<kRms, 2, 8, 12, 1, 2, false>(q, s)
                                    : launch_ring<kRms, 2, 8, 8, 1, 2, false>(q, s);
-    case 6144: return launch_ring<kRms, 3, 8, 12, 3, 1, false>(q, s);
+    case 6144: return launch_ring<kRms, 3, 8, 12, 3, 2, false>(q, s);
     default: return launch_ring<kRms, 4, 8, 16, 4, 1, false>(q, s); // 8192: 4 warps per row
     }
 }
