@@ -169,32 +169,31 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
         return;
     }
 
-    // The lane's columns widened to fp32 once; packed operations take two
-    // neighbouring columns throughout.
-    float x[kHeadsPerLane][8];
+    // The lane's columns widened to fp32 once, as pairs of heads: x2[j][e]
+    // holds column e of heads 2j and 2j+1, so the packed operations of the
+    // squares and of the normalisation each serve two heads.
+    constexpr int NP = kHeadsPerLane / 2;
+    float2 x2[NP][8];
 #pragma unroll
-    for (int k = 0; k < kHeadsPerLane; ++k)
+    for (int j = 0; j < NP; ++j)
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            x[k][2 * m] = lo_f(word(U.x[k], m));
-            x[k][2 * m + 1] = hi_f(word(U.x[k], m));
+            const uint32_t a = word(U.x[2 * j], m), b = word(U.x[2 * j + 1], m);
+            x2[j][2 * m] = make_float2(lo_f(a), lo_f(b));
+            x2[j][2 * m + 1] = make_float2(hi_f(a), hi_f(b));
         }
 
     // Partial sum of squares of each of the lane's heads over its 8 columns:
-    // one ordered chain per head (two products per packed multiply, added
-    // in column order).
+    // one ordered chain per head, rn(acc + rn(x * x)) in column order, two
+    // heads per packed operation.
     float ps[16];
 #pragma unroll
-    for (int k = 0; k < kHeadsPerLane; ++k) {
-        float acc = 0.0f;
+    for (int j = 0; j < NP; ++j) {
+        float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            const float2 x2 = make_float2(x[k][e], x[k][e + 1]);
-            const float2 sq = mul2(x2, x2);
-            acc = __fadd_rn(acc, sq.x);
-            acc = __fadd_rn(acc, sq.y);
-        }
-        ps[k] = acc;
+        for (int e = 0; e < 8; ++e) acc = addmul2(acc, x2[j][e], x2[j][e]);
+        ps[2 * j] = acc.x;
+        ps[2 * j + 1] = acc.y;
     }
 #pragma unroll
     for (int k = kHeadsPerLane; k < 16; ++k) ps[k] = 0.0f;
@@ -219,9 +218,12 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
     for (int j = 0; j < S::NK; ++j)
         my_rstd[j] = defined_rsqrt(__fadd_rn(div_by<HD>(ps[j]), p.eps[U.s_]));
 
-    float2 w2[4], cc[4], sn[4];
+    float2 wd[8], cc[4], sn[4]; // wd[e]: weight of column e, duplicated
 #pragma unroll
-    for (int m = 0; m < 4; ++m) w2[m] = wide2(word(U.w, m));
+    for (int m = 0; m < 4; ++m) {
+        wd[2 * m] = dup2(lo_f(word(U.w, m)));
+        wd[2 * m + 1] = dup2(hi_f(word(U.w, m)));
+    }
     const bool first = fl < S::LPH / 2; // neox: the lane holds the first half's columns
     if (NEOX) {
         // columns (2m, 2m+1) of the lane: cos pairs and sin pairs, the sin
@@ -241,18 +243,9 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
         }
     }
     const int lane_base = hs * S::LPH;
-#pragma unroll
-    for (int k = 0; k < kHeadsPerLane; ++k) {
-        const float rstd = __shfl_sync(kFull, my_rstd[k % S::NK], lane_base + brev<S::LEVELS>(k / S::NK));
-        if (U.h0 + S::GPS * k >= p.H) break; // warp-uniform: no head left in any slot
-        const int h = U.h0 + hs + S::GPS * k;
-        const float2 r2 = dup2(rstd);
-        uint32_t nw[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float2 t2 = mul2(mul2(make_float2(x[k][2 * m], x[k][2 * m + 1]), r2), w2[m]);
-            nw[m] = pack_bf16(t2.x, t2.y); // normalised, rounded to bf16
-        }
+    // Rotate the bf16 row nw of head h (this lane's four column pairs) and
+    // store it.
+    auto rotate_store = [&](const uint32_t (&nw)[4], int h) {
         uint4 out;
         if (NEOX) {
 #pragma unroll
@@ -272,6 +265,26 @@ __device__ __forceinline__ void qk_process(const QkUnit &U, const QkParams &p, i
             }
         }
         if (h < p.H) st_stream(dst + h * S::LPH + fl, out);
+    };
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        const int k0 = 2 * j, k1 = 2 * j + 1;
+        const float r0 = __shfl_sync(kFull, my_rstd[k0 % S::NK], lane_base + brev<S::LEVELS>(k0 / S::NK));
+        const float r1 = __shfl_sync(kFull, my_rstd[k1 % S::NK], lane_base + brev<S::LEVELS>(k1 / S::NK));
+        if (U.h0 + S::GPS * k0 >= p.H) break; // warp-uniform: no head left in any slot
+        const float2 r2 = make_float2(r0, r1);
+        // normalised, rounded to bf16: nw0 for head 2j, nw1 for head 2j+1
+        uint32_t nw0[4], nw1[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float2 te = mul2(mul2(x2[j][2 * m], r2), wd[2 * m]);
+            const float2 to = mul2(mul2(x2[j][2 * m + 1], r2), wd[2 * m + 1]);
+            nw0[m] = pack_bf16(te.x, to.x);
+            nw1[m] = pack_bf16(te.y, to.y);
+        }
+        rotate_store(nw0, U.h0 + hs + S::GPS * k0);
+        if (U.h0 + S::GPS * k1 >= p.H) break;
+        rotate_store(nw1, U.h0 + hs + S::GPS * k1);
     }
 }
 
