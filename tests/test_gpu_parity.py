@@ -433,3 +433,10 @@ def test_gated_residual_transposed_shapes(B, D, T):
 def test_gated_residual_transposed_in_place_and_site():
     run_resid_t(1, 3072, 4096, 710, inplace=True)
     run_resid_t(2, 3072, 512, 711)
+
+
+def test_gated_residual_transposed_tile_runs_cross_batches():
+    """More tiles than resident CTAs, with ragged channel and token tiles:
+    a CTA's run of tiles crosses a batch boundary and reuses its stages."""
+    run_resid_t(2, 1032, 1800, 712)
+    run_resid_t(2, 1032, 1800, 713, inplace=True)
