@@ -664,12 +664,14 @@ def config_bytes(kind, B, T, D, weight):
     return io * rows * D + nvec * B * D * 2 + (D * 2 if weight else 0), rows
 
 
-def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20, eager_only=0):
+def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_repeats=10, eager_only=0):
     """Launch time of every configuration: a graph of launches cycling over
     enough buffer sets that ~2x L2 of other traffic separates two uses of a
     buffer (up to max_sets; smaller configurations stay L2-resident and say
     so).  Inputs are drawn on the device (normal, seeded): the kernels'
-    time does not depend on the values.  eager_only = k > 0 instead runs
+    time does not depend on the values.  Each configuration is timed as
+    n_repeats repeats of at least 100 launches; the median repeat is
+    reported, with the fastest and slowest.  eager_only = k > 0 instead runs
     each configuration k times without graphs or timing (for an ncu
     capture of every configuration's DRAM traffic) and returns None."""
     import torch
@@ -754,11 +756,16 @@ def time_configs(dev, stream, min_bytes=260 << 20, max_sets=16, n_iter=20, eager
             for _ in range(3):
                 graph.replay()
             torch.cuda.synchronize()
-            el = time_graphs([graph], n_iter, stream)
-        us = el / (n_iter * reps) * 1e6
+            # repeats of >= 100 launches each; the median repeat is reported
+            per = -(-100 // reps)
+            samples = [time_graphs([graph], per, stream) / (per * reps) * 1e6
+                       for _ in range(n_repeats)]
+        us = statistics.median(samples)
         out[name] = {"us_per_launch": us, "gbs": nbytes / us / 1e3, "rows_per_s": rows / us * 1e6,
                      "bytes_per_launch": nbytes, "rows_per_launch": rows, "buffer_sets": nsets,
-                     "l2_resident": nsets * nbytes < min_bytes}
+                     "l2_resident": nsets * nbytes < min_bytes, "repeats": n_repeats,
+                     "launches_per_repeat": per * reps,
+                     "us_min_max": [round(min(samples), 3), round(max(samples), 3)]}
         del sets, graph
         torch.cuda.empty_cache()
     return None if eager_only else out
