@@ -170,3 +170,33 @@ def test_qk_variant_token_subsets(hd, neox):
     part = run(Pt[5:40], Pi[17:250], RT[5:40].contiguous(), RI[17:250].contiguous())
     for g, f in zip(part, full):
         assert_bits_equal(g, np.concatenate([f[5:40], f[Tt + 17:Tt + 250]]), "qk variant slices")
+
+
+@pytest.mark.parametrize("kind", ["ln", "rms", "gated", "ln_fp8", "gated_ln"])
+def test_launch_shape_invariance(kind):
+    """Rows 100..163 of a [1, 4216, 4096] launch (twelve warps per CTA, many
+    rows per SM) and the same rows as a [1, 64, 4096] launch (eight warps,
+    one row or none per warp) give the same bits."""
+    Dm, Tm, lo, hi = 4096, 4216, 100, 164
+    x = synth.normal_bf16((1, Tm, Dm), 31)
+    h = synth.normal_bf16((1, Tm, Dm), 32)
+    vec = to_dev(synth.normal_bf16((1, 6 * Dm), 33, 0.2))
+    sc, sh, g = vec[:, :Dm], vec[:, Dm:2 * Dm], vec[:, 2 * Dm:3 * Dm]
+
+    def run(xx, hh):
+        if kind == "ln":
+            return [ops.ln_modulate(xx, sc, sh, EPS)]
+        if kind == "rms":
+            return [ops.rms_modulate(xx, sc, sh, EPS)]
+        if kind == "ln_fp8":
+            return [ops.ln_modulate_fp8(xx, sc, sh, 0.05, EPS)]
+        if kind == "gated":
+            return list(ops.gated_rms_modulate(xx, hh, g, sc, sh, EPS))
+        return list(ops.gated_ln_modulate(xx, hh, g, sc, sh, EPS))
+
+    big = run(to_dev(x), to_dev(h))
+    small = run(to_dev(np.ascontiguousarray(x[:, lo:hi])), to_dev(np.ascontiguousarray(h[:, lo:hi])))
+    for i, (a, b) in enumerate(zip(big, small)):
+        a = a.cpu().view(torch.int16).numpy() if a.dtype == torch.bfloat16 else a.cpu().numpy()
+        b = b.cpu().view(torch.int16).numpy() if b.dtype == torch.bfloat16 else b.cpu().numpy()
+        assert np.array_equal(a[:, lo:hi], b), f"{kind} output {i}: launch shape changed the bits"

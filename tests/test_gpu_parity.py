@@ -164,6 +164,12 @@ def test_ln_metric_shape():
     run_ln(1, 4216, 4096, synth.SEED_X, outliers=True)
 
 
+def test_ln_flux_cfg_site_odd_tokens():
+    """The FLUX LayerNorm test's CFG case: [2, 300, 3072], x = N(0,1) * 8,
+    scale/shift chunk views of a 6-chunk embedding."""
+    run_ln(2, 300, 3072, 403, x_bits=synth.normal_bf16((2, 300, 3072), 403, 8.0), chunks=6)
+
+
 # ------------------------------------------------------------ edge cases
 
 def _special_rows(D, seed):
