@@ -40,7 +40,7 @@ struct QkParams {
 };
 
 constexpr int kQkNW = 8;  // warps per CTA (measured best among 4..16)
-constexpr int kQkSPC = 1; // slots per warp
+constexpr int kQkSPC = 1; // slots per warp (two to four, at 4 to 12 warps, were slower)
 constexpr int kHeadsPerLane = 12; // head fragments a lane holds per unit
 
 // Shape of the work for head_dim HD.
