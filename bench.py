@@ -651,6 +651,7 @@ CONFIGS = [
     ("N3 qk 256+4096 tokens x 48 heads x 64", "qk", 1, 0, 64, False),
     ("N3 qk neox 256+4096 tokens x 48 heads x 64", "qk", 1, 0, 64, True),
     ("N2 gated residual, [1,3072,4096] residual layout", "resid_t", 1, 4096, 3072, False),
+    ("N2 gated residual, [1,3072,4093] residual layout (odd T)", "resid_t", 1, 4093, 3072, False),
 ]
 
 

@@ -24,8 +24,9 @@
 // product bf16(gate * h) is formed on channel pairs, as the update holds
 // them, and regrouped into token pairs with byte permutes before the add.
 //
-// Other T: 64 x 64 tiles, one per CTA, element by element on the residual
-// (its rows are not 16-byte aligned).
+// Other T (residual rows not 16-byte aligned): one 64 x 64 tile per CTA,
+// token pairs on 4-byte boundaries with the lanes of a warp on consecutive
+// pairs, the residual words loaded together with the update tile.
 #include "dan_device.cuh"
 #include "dan_internal.h"
 #include "dan_ring.cuh"
@@ -35,7 +36,8 @@ namespace dan {
 namespace {
 
 constexpr int kTile = 64;          // channels and tokens per tile
-constexpr int kResidThreads = 128; // 16 channel quads x 8 token octets
+constexpr int kResidThreads = 128; // four warps per 64 x 64 tile
+constexpr int kResidCtas = 8;      // resident CTAs per SM the register budget allows
 
 struct ResidParams {
     const uint16_t *r;
@@ -50,44 +52,36 @@ struct ResidParams {
 __device__ __forceinline__ uint32_t lows(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5410); }
 __device__ __forceinline__ uint32_t highs(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
 
-// Tile order: within a batch, bands of kBand token tiles; in a band, the
-// channel tiles, and in each channel tile the band's token tiles, so the
-// tiles in flight at once cover whole update rows and runs of each
-// residual row.
-constexpr unsigned kBand = 16;
-
 struct TileAt {
     unsigned b, d0, t0;
 };
 
-__device__ __forceinline__ TileAt tile_at(const ResidParams &p, unsigned tile)
+// Tile i of the (batch, channel tile, token tile) order, tokens fastest,
+// for tiles of kTile tokens.
+__device__ __forceinline__ TileAt tile_at(const ResidParams &p, unsigned i)
 {
-    const unsigned per_b = p.tiles_d * p.tiles_t;
-    const unsigned b = tile / per_b, rem = tile - b * per_b;
-    const unsigned full = p.tiles_t / kBand, in_full = full * kBand * p.tiles_d;
-    unsigned dt, tt;
-    if (rem < in_full) {
-        const unsigned band = rem / (kBand * p.tiles_d), r2 = rem - band * (kBand * p.tiles_d);
-        dt = r2 / kBand;
-        tt = band * kBand + (r2 - dt * kBand);
-    } else { // the last, narrower band
-        const unsigned w = p.tiles_t - full * kBand, r2 = rem - in_full;
-        dt = r2 / w;
-        tt = full * kBand + (r2 - dt * w);
-    }
+    const unsigned tt = i % p.tiles_t, rest = i / p.tiles_t;
+    const unsigned dt = rest % p.tiles_d, b = rest / p.tiles_d;
     return TileAt{b, dt * kTile, tt * kTile};
 }
 
-// One 64 x 64 tile per CTA, element by element on the residual (any T).
-__global__ void __launch_bounds__(kResidThreads) gated_residual_t_kernel(const ResidParams p)
+// Any T: one 64 x 64 tile per CTA of 128 threads (tokens fastest in
+// the grid), up to kResidCtas CTAs per SM.  The update tile sits
+// in shared memory at a pitch of 33 words; each warp walks channel rows,
+// lane k on the k-th 4-byte-aligned token pair of the row's segment (so a
+// warp's residual loads and stores cover 128 contiguous bytes), with single
+// elements, as 2-byte accesses, where a segment starts or ends off a pair.
+__global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_kernel(const ResidParams p)
 {
-    __shared__ __align__(16) uint2 s_h[kTile][kTile / 4]; // update tile: [token][channel quad]
+    constexpr int kPitchW = kTile / 2 + 1; // words per update row: 32 channel pairs + 1
+    __shared__ uint32_t s_h[kTile * kPitchW]; // update tile: [token][channel pair]
+    __shared__ uint32_t s_g[kTile];           // gate of each channel (low half)
 
     grid_dependency_wait(); // no global access above this line
     allow_dependents();
-    const TileAt at = tile_at(p, blockIdx.x);
     const int64_t T = p.T, D = p.D;
     const int tid = threadIdx.x;
+    const TileAt at = tile_at(p, blockIdx.x);
 
     // Update tile: 64 rows x 8 chunks of 16 bytes; chunks outside the
     // tensor read as zero (their products are never stored).
@@ -100,40 +94,58 @@ __global__ void __launch_bounds__(kResidThreads) gated_residual_t_kernel(const R
             const int row = (tid >> 3) + 16 * j;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (col_in && (int64_t)at.t0 + row < T) v = ld_stream(h + (int64_t)row * (D / 8));
-            reinterpret_cast<uint4 *>(&s_h[row][0])[ch] = v;
+            uint32_t *dst = s_h + row * kPitchW + 4 * ch;
+            dst[0] = v.x;
+            dst[1] = v.y;
+            dst[2] = v.z;
+            dst[3] = v.w;
         }
+    }
+    if (tid < kTile) {
+        const int64_t d = (int64_t)at.d0 + tid;
+        s_g[tid] = d < D ? (uint32_t)p.gate[(int64_t)at.b * p.vs + d] : 0u;
+    }
+
+    // Token pairs on 4-byte boundaries: (2k, 2k+1) when a row segment starts
+    // on one, else (2k+1, 2k+2) and token 0 alone.  The residual words are
+    // loaded before the barrier, so they are in flight with the update tile.
+    const int warp = tid >> 5, lane = tid & 31;
+    const int nt = (int)(T - at.t0 < kTile ? T - at.t0 : kTile); // tokens of the tile
+    constexpr int kRows = kTile / 4;                               // channel rows per warp
+    uint32_t rw[kRows], r0[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        const int dl = warp + 4 * j;
+        rw[j] = r0[j] = 0u;
+        if ((int64_t)at.d0 + dl >= D) continue;
+        const int64_t rb = ((int64_t)at.b * D + at.d0 + dl) * T + at.t0; // r[b][d][t0]
+        const int odd = (int)(rb & 1), t = 2 * lane + odd;
+        if (t + 1 < nt) rw[j] = *reinterpret_cast<const uint32_t *>(p.r + rb + t);
+        else if (t < nt) rw[j] = p.r[rb + t];
+        if (odd && lane == 0) r0[j] = p.r[rb];
     }
     __syncthreads();
 
-    const int cq = tid & 15, tg = tid >> 4;   // channels 4cq..4cq+3, tokens 8tg..8tg+7
-    const int64_t d = (int64_t)at.d0 + 4 * cq; // D % 4 == 0: whole quad in or out
-    const int64_t t = (int64_t)at.t0 + 8 * tg;
-    if (d >= D || t >= T) return;
-    const int64_t rrow = ((int64_t)at.b * D + d) * T + t; // element index of r[b][d][t]
-    const uint2 g = *reinterpret_cast<const uint2 *>(p.gate + (int64_t)at.b * p.vs + d);
-    // gh on channel pairs: gh[k] = (channels 4cq, 4cq+1), gh[8+k] = (4cq+2, 4cq+3) of token t+k
-    uint32_t gh[16];
+    // update element of token tl, channel dl (low half)
+    auto hval = [&](int tl, int dl) -> uint32_t {
+        const uint32_t hw = s_h[tl * kPitchW + (dl >> 1)];
+        return (dl & 1) ? hw >> 16 : hw & 0xFFFFu;
+    };
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint2 hv = s_h[8 * tg + k][cq];
-        gh[k] = hmul2(g.x, hv.x);
-        gh[8 + k] = hmul2(g.y, hv.y);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            // channel c, tokens (2q, 2q+1): low (c even) or high halves
-            const uint32_t a = gh[8 * (c >> 1) + 2 * q], b = gh[8 * (c >> 1) + 2 * q + 1];
-            const uint32_t ghw = (c & 1) ? highs(a, b) : lows(a, b);
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-                if (t + 2 * q + e < T) {
-                    const int64_t i = rrow + c * T + 2 * q + e;
-                    const uint32_t w = hadd2((uint32_t)p.r[i], e ? ghw >> 16 : ghw & 0xFFFFu);
-                    p.r_out[i] = (uint16_t)w;
-                }
+    for (int j = 0; j < kRows; ++j) {
+        const int dl = warp + 4 * j; // channel within the tile
+        if ((int64_t)at.d0 + dl >= D) break; // warp-uniform
+        const uint32_t g = s_g[dl], g2 = g | (g << 16);
+        const int64_t rb = ((int64_t)at.b * D + at.d0 + dl) * T + at.t0;
+        const int odd = (int)(rb & 1), t = 2 * lane + odd;
+        if (t + 1 < nt) {
+            const uint32_t h2 = hval(t, dl) | (hval(t + 1, dl) << 16);
+            *reinterpret_cast<uint32_t *>(p.r_out + rb + t) = gated_word(rw[j], g2, h2);
+        } else if (t < nt) {
+            p.r_out[rb + t] = (uint16_t)gated_word(rw[j], g, hval(t, dl));
         }
+        if (odd && lane == 0) p.r_out[rb] = (uint16_t)gated_word(r0[j], g, hval(0, dl));
+    }
 }
 
 // ------------------------------------------------ the pipelined kernel
