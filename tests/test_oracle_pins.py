@@ -592,6 +592,31 @@ def test_ln_fp8_is_quantised_ln_modulate(orc):
                               want.view(torch.uint8).numpy())
 
 
+def test_ln_fp8_scale_applied_as_reciprocal_multiply(orc):
+    """The static scale is applied as rn(y * rn(1/qscale)), the reading the
+    FP8 producer is built on, not as rn(y / qscale): at qscale = 7 the two
+    round to different E4M3 codes for some bf16 y.  Constant rows make y
+    equal to shift exactly (scale = 0, so bf16(1 + scale) = 1)."""
+    bits = np.arange(0x0001, 0x7F80, dtype=np.uint32)
+    yv = (bits << 16).view(np.float32)
+    yv = yv[yv < 448.0 * 7.0]
+    qs = np.float32(7.0)
+    mul = torch.from_numpy(yv * (np.float32(1.0) / qs)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    div = torch.from_numpy(yv / qs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    split = yv[mul != div]
+    assert split.size > 0  # the two readings differ somewhere
+    D = 8 * ((split.size + 7) // 8)
+    shift = np.zeros((1, D), np.float32)
+    shift[0, :split.size] = split
+    shift_bits = bits_of(shift)
+    x = bits_of(np.full((1, 3, D), 1.5, np.float32))
+    scale = bits_of(np.zeros((1, D), np.float32))
+    q = orc.ln_modulate_fp8(x, scale, shift_bits, 7.0, EPS)
+    want = torch.from_numpy(widen(shift_bits) * (np.float32(1.0) / qs)).to(torch.float8_e4m3fn)
+    assert np.array_equal(q, np.broadcast_to(want.view(torch.uint8).numpy()[:, None, :], (1, 3, D)))
+    assert not np.array_equal(q[0, 0, :split.size], div[mul != div])
+
+
 # ---------------------------------------------- gated residual + LayerNorm
 
 def test_gated_ln_residual_and_composition(orc):
