@@ -272,6 +272,31 @@ def run_qk(Tt, Ti, H, seed, packed=True, eps=(1e-6, 1e-6), hd=128, neox=False):
         assert_bits_equal(from_dev(g), w, f"qk {name} Tt={Tt} Ti={Ti} H={H} hd={hd} neox={neox}")
 
 
+@pytest.mark.parametrize("hd", [128, 64])
+def test_qk_head_fold_order_case(hd):
+    """Heads whose sum depends on the fold order (thread 0's partial 2^24,
+    the others 1: the adjacent-pair tree keeps the 1s a left-to-right sum
+    loses), among random heads."""
+    H, Tt, Ti = 24 * 128 // hd, 3, 5
+    pt, pi = synth.packed_qkv(Tt, H, 640, hd), synth.packed_qkv(Ti, H, 641, hd)
+    special = np.zeros(hd, np.float32)
+    special[0] = 4096.0
+    special[8::8] = 1.0
+    for arr in (pt, pi):
+        for h in range(0, 2 * H, 3):  # every third Q/K head
+            arr[:, h * hd:(h + 1) * hd] = synth.to_bf16_bits(special)
+    ws = [synth.to_bf16_bits(np.ones(hd, np.float32))] * 4
+    rt, ri = synth.rope_table(Tt, hd), synth.rope_table(Ti, hd, pos0=Tt)
+    Pt, Pi = to_dev(pt), to_dev(pi)
+    outs = ops.qk_norm_rope_epilogue(synth.split_qkv(Pt, H, hd), synth.split_qkv(Pi, H, hd),
+                                     *[to_dev(w) for w in ws], torch.from_numpy(rt).cuda(),
+                                     torch.from_numpy(ri).cuda(), 0.0, 0.0, H, head_dim=hd)
+    want = oracle.qk_norm_rope_epilogue(synth.split_qkv(pt, H, hd), synth.split_qkv(pi, H, hd),
+                                        H, ws, rt, ri, 0.0, 0.0, head_dim=hd)
+    for name, g, w in zip("qkv", outs, want):
+        assert_bits_equal(from_dev(g), w, f"qk fold-order case {name} hd={hd}")
+
+
 @pytest.mark.parametrize("H", [24, 3, 1, 30])
 @pytest.mark.parametrize("packed", [True, False])
 def test_qk_small(H, packed):

@@ -737,3 +737,32 @@ def test_gated_residual_transposed_against_torch(orc):
     one = orc.gated_residual_transposed(r, h, vec(B, D, 1.0))
     exact = widen(r).astype(np.float64) + np.swapaxes(widen(h), 1, 2).astype(np.float64)
     assert np.array_equal(widen(one), bf16_of_f64(exact).astype(np.float32))
+
+
+@pytest.mark.parametrize("hd,tree_s", [(128, 16777230.0), (64, 16777222.0)])
+def test_qk_head_fold_is_adjacent_pair_tree(orc, hd, tree_s):
+    """The head sum folds the hd/8 logical threads' partials by the
+    adjacent-pair tree (guide, canonical RMS order; one 8-column chain per
+    thread).  Worked by hand: column 0 = 4096 gives thread 0 the partial
+    2^24, and column 8l = 1 gives thread l >= 1 the partial 1.  The tree
+    adds (2^24 + 1) -> 2^24 (tie to even), then 2^24 + 2, + 4, + 8 for 16
+    threads (16777230) or + 2, + 4 for 8 (16777222); a left-to-right sum
+    would lose every 1 and give 2^24."""
+    H, Tt, Ti = 2, 1, 1
+    row = np.zeros(3 * H * hd, np.float32)
+    for h in range(2 * H):  # every Q and K head
+        base = h * hd
+        row[base] = 4096.0
+        row[base + 8:base + hd:8] = 1.0
+    packed = bits_of(np.stack([row, row]))
+    ones = [bits_of(np.ones(hd))] * 4
+    eps = 0.0
+    _, _, _, rs = orc.qk_norm_rope_epilogue(
+        synth.split_qkv(packed[:Tt], H, hd), synth.split_qkv(packed[Tt:], H, hd), H, ones,
+        _rope_const_hd(Tt, hd, 1, 0), _rope_const_hd(Ti, hd, 1, 0), eps, eps, with_stats=True,
+        head_dim=hd)
+    f = np.float32
+    want = f(1.0) / np.sqrt(f(tree_s) / f(hd))            # s/hd exact (power of two), eps = 0
+    seq = f(1.0) / np.sqrt(f(2.0 ** 24) / f(hd))
+    assert want != seq
+    assert np.all(rs == want), (rs, want)
