@@ -24,9 +24,11 @@
 // product bf16(gate * h) is formed on channel pairs, as the update holds
 // them, and regrouped into token pairs with byte permutes before the add.
 //
-// Other T (residual rows not 16-byte aligned): one 64 x 64 tile per CTA,
-// token pairs on 4-byte boundaries with the lanes of a warp on consecutive
-// pairs, the residual words loaded together with the update tile.
+// Other T (residual rows not 16-byte aligned): one 64-channel tile per
+// CTA, each row parity on the 64 tokens whose pairs are 4-byte aligned; the
+// products are formed on the update's channel pairs and stored transposed
+// in shared memory, so the lanes of a warp take consecutive whole token
+// pairs with one aligned shared load each.
 #include "dan_device.cuh"
 #include "dan_internal.h"
 #include "dan_ring.cuh"
@@ -65,86 +67,106 @@ __device__ __forceinline__ TileAt tile_at(const ResidParams &p, unsigned i)
     return TileAt{b, dt * kTile, tt * kTile};
 }
 
-// Any T: one 64 x 64 tile per CTA of 128 threads (tokens fastest in
-// the grid), up to kResidCtas CTAs per SM.  The update tile sits
-// in shared memory at a pitch of 33 words; each warp walks channel rows,
-// lane k on the k-th 4-byte-aligned token pair of the row's segment (so a
-// warp's residual loads and stores cover 128 contiguous bytes), with single
-// elements, as 2-byte accesses, where a segment starts or ends off a pair.
+// Any T: one 64-channel tile per CTA of 128 threads (tokens fastest in the
+// grid), up to kResidCtas CTAs per SM.  Residual row (b, d) starts at
+// element (b*D + d)*T; D and the tile origins t0 are even, so a row starts
+// on an odd element exactly when T and d are both odd.  Each row parity
+// takes the 64 tokens whose pairs sit on 4-byte boundaries: [t0, t0 + 64)
+// for even rows, [t0 - 1, t0 + 63) for odd ones, so inside the tensor every
+// lane of a warp moves one whole aligned pair per row, and single elements
+// (2-byte accesses) occur only at the ends of a residual row.  The update
+// rows t0 - (T odd) .. t0 + 63 are multiplied by the gate in their own
+// layout (channel pairs of one token), and the products bf16(gate * h) are
+// stored transposed in shared memory, one row of 64 tokens per channel in
+// that channel's token range, so lane k's pair is word k of the row
+// (conflict-free).  A warp walks channel rows w, w+4, ... (all of one
+// parity); the residual words are loaded first, so they are in flight with
+// the update tile.
 __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_kernel(const ResidParams p)
 {
-    constexpr int kPitchW = kTile / 2 + 1; // words per update row: 32 channel pairs + 1
-    __shared__ uint32_t s_h[kTile * kPitchW]; // update tile: [token][channel pair]
-    __shared__ uint32_t s_g[kTile];           // gate of each channel (low half)
+    constexpr int kPitchW = kTile / 2 + 1; // words per product row (32 used)
+    constexpr int kRows = kTile / 4;       // channel rows per warp
+    __shared__ uint32_t s_p[kTile * kPitchW + 4];
+    uint16_t *s_p16 = reinterpret_cast<uint16_t *>(s_p);
+    // First word of channel ch's product row; the upper 32 rows move by four
+    // banks, so the eight channel octets of a transposing store hit eight
+    // different bank groups.
+    auto prow = [](int ch) { return ch * kPitchW + (ch >= kTile / 2 ? 4 : 0); };
 
     grid_dependency_wait(); // no global access above this line
     allow_dependents();
     const int64_t T = p.T, D = p.D;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const TileAt at = tile_at(p, blockIdx.x);
+    const int64_t t0 = at.t0;
+    const int nd = (int)(D - at.d0 < kTile ? D - at.d0 : kTile); // channels of the tile
+    const int todd = (int)(T & 1);
+    const int odd = warp & todd;   // parity of this warp's rows
+    const int e = 2 * lane - odd;  // this lane's pair: tokens t0 + e, t0 + e + 1
+    const bool lo_ok = t0 + e >= 0 && t0 + e < T;
+    const bool hi_ok = t0 + e + 1 < T;
+    const int64_t rstep = 4 * T;   // elements between two rows of a warp
+    const int64_t base = ((int64_t)at.b * D + at.d0 + warp) * T + t0 + e; // r[b][d0 + warp][t0 + e]
 
-    // Update tile: 64 rows x 8 chunks of 16 bytes; chunks outside the
-    // tensor read as zero (their products are never stored).
+    uint32_t rw[kRows];
     {
-        const int ch = tid & 7;
-        const bool col_in = (int64_t)at.d0 + 8 * ch < D; // D % 8 == 0: whole chunk
-        const uint4 *h = p.h + (((int64_t)at.b * T + at.t0) * D + at.d0) / 8 + ch;
+        const uint16_t *q = p.r + base;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int row = (tid >> 3) + 16 * j;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (col_in && (int64_t)at.t0 + row < T) v = ld_stream(h + (int64_t)row * (D / 8));
-            uint32_t *dst = s_h + row * kPitchW + 4 * ch;
-            dst[0] = v.x;
-            dst[1] = v.y;
-            dst[2] = v.z;
-            dst[3] = v.w;
+        for (int j = 0; j < kRows; ++j, q += rstep) {
+            rw[j] = 0u;
+            if (warp + 4 * j >= nd) continue; // warp-uniform
+            if (lo_ok && hi_ok) rw[j] = *reinterpret_cast<const uint32_t *>(q);
+            else if (lo_ok) rw[j] = q[0];
+            else if (hi_ok) rw[j] = (uint32_t)q[1] << 16;
         }
     }
-    if (tid < kTile) {
-        const int64_t d = (int64_t)at.d0 + tid;
-        s_g[tid] = d < D ? (uint32_t)p.gate[(int64_t)at.b * p.vs + d] : 0u;
-    }
 
-    // Token pairs on 4-byte boundaries: (2k, 2k+1) when a row segment starts
-    // on one, else (2k+1, 2k+2) and token 0 alone.  The residual words are
-    // loaded before the barrier, so they are in flight with the update tile.
-    const int warp = tid >> 5, lane = tid & 31;
-    const int nt = (int)(T - at.t0 < kTile ? T - at.t0 : kTile); // tokens of the tile
-    constexpr int kRows = kTile / 4;                               // channel rows per warp
-    uint32_t rw[kRows], r0[kRows];
+    // Products: thread (channel octet c, update rows tid/8 + 16m), update row
+    // hr holding token t0 - todd + hr; D % 8 == 0, so an octet is wholly
+    // inside or outside the tensor.  A token's product goes to index
+    // hr - todd of an even channel's row and hr of an odd channel's.
+    {
+        const int c = tid & 7;
+        if (8 * c < nd) {
+            const int64_t dc = (int64_t)at.d0 + 8 * c;
+            const uint4 g = ld_vec(reinterpret_cast<const uint4 *>(p.gate + (int64_t)at.b * p.vs + dc));
+            const uint4 *h = p.h + ((int64_t)at.b * T * D + dc) / 8;
+            const int64_t tb = t0 - todd;
+            constexpr int kPasses = kTile / 16 + 1;
+            uint4 hv[kPasses];
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-        const int dl = warp + 4 * j;
-        rw[j] = r0[j] = 0u;
-        if ((int64_t)at.d0 + dl >= D) continue;
-        const int64_t rb = ((int64_t)at.b * D + at.d0 + dl) * T + at.t0; // r[b][d][t0]
-        const int odd = (int)(rb & 1), t = 2 * lane + odd;
-        if (t + 1 < nt) rw[j] = *reinterpret_cast<const uint32_t *>(p.r + rb + t);
-        else if (t < nt) rw[j] = p.r[rb + t];
-        if (odd && lane == 0) r0[j] = p.r[rb];
+            for (int m = 0; m < kPasses; ++m) {
+                const int hr = (tid >> 3) + 16 * m;
+                const int64_t tk = tb + hr;
+                hv[m] = make_uint4(0, 0, 0, 0);
+                if (hr < kTile + todd && tk >= 0 && tk < T) hv[m] = ld_stream(h + tk * (D / 8));
+            }
+#pragma unroll
+            for (int m = 0; m < kPasses; ++m) {
+                const int hr = (tid >> 3) + 16 * m;
+                if (hr >= kTile + todd) continue;
+                const int ie = hr - todd, io = hr;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const uint32_t pr = hmul2(word(g, w), word(hv[m], w));
+                    const int ch = 8 * c + 2 * w;
+                    if (ie >= 0 && ie < kTile) s_p16[2 * prow(ch) + ie] = (uint16_t)pr;
+                    if (io < kTile) s_p16[2 * prow(ch + 1) + io] = (uint16_t)(pr >> 16);
+                }
+            }
+        }
     }
     __syncthreads();
 
-    // update element of token tl, channel dl (low half)
-    auto hval = [&](int tl, int dl) -> uint32_t {
-        const uint32_t hw = s_h[tl * kPitchW + (dl >> 1)];
-        return (dl & 1) ? hw >> 16 : hw & 0xFFFFu;
-    };
+    uint16_t *q = p.r_out + base;
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-        const int dl = warp + 4 * j; // channel within the tile
-        if ((int64_t)at.d0 + dl >= D) break; // warp-uniform
-        const uint32_t g = s_g[dl], g2 = g | (g << 16);
-        const int64_t rb = ((int64_t)at.b * D + at.d0 + dl) * T + at.t0;
-        const int odd = (int)(rb & 1), t = 2 * lane + odd;
-        if (t + 1 < nt) {
-            const uint32_t h2 = hval(t, dl) | (hval(t + 1, dl) << 16);
-            *reinterpret_cast<uint32_t *>(p.r_out + rb + t) = gated_word(rw[j], g2, h2);
-        } else if (t < nt) {
-            p.r_out[rb + t] = (uint16_t)gated_word(rw[j], g, hval(t, dl));
-        }
-        if (odd && lane == 0) p.r_out[rb] = (uint16_t)gated_word(r0[j], g, hval(0, dl));
+    for (int j = 0; j < kRows; ++j, q += rstep) {
+        const int dl = warp + 4 * j;
+        if (dl >= nd) break; // warp-uniform
+        const uint32_t v = hadd2(rw[j], s_p[prow(dl) + lane]);
+        if (lo_ok && hi_ok) *reinterpret_cast<uint32_t *>(q) = v;
+        else if (lo_ok) q[0] = (uint16_t)v;
+        else if (hi_ok) q[1] = (uint16_t)(v >> 16);
     }
 }
 

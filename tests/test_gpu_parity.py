@@ -456,7 +456,8 @@ def run_resid_t(B, D, T, seed, inplace=False):
 
 @pytest.mark.parametrize("B,D,T", [(1, 8, 1), (1, 72, 37), (2, 64, 64), (1, 136, 130),
                                    (2, 3072, 97), (1, 256, 4093), (1, 8, 8), (1, 72, 136),
-                                   (2, 200, 8), (3, 520, 72)])
+                                   (2, 200, 8), (3, 520, 72), (1, 8, 3), (1, 16, 2),
+                                   (3, 24, 65), (1, 64, 63), (2, 40, 127), (1, 1032, 4094)])
 def test_gated_residual_transposed_shapes(B, D, T):
     run_resid_t(B, D, T, 700 + D + T)
 
@@ -471,3 +472,14 @@ def test_gated_residual_transposed_tile_runs_cross_batches():
     a CTA's run of tiles crosses a batch boundary and reuses its stages."""
     run_resid_t(2, 1032, 1800, 712)
     run_resid_t(2, 1032, 1800, 713, inplace=True)
+
+
+def test_gated_residual_transposed_odd_tokens():
+    """T odd: the residual rows of odd channels start on odd elements, so the
+    tile's token pairs and its single edge tokens change with the channel;
+    in place, across batches with ragged tiles, and at the [1,3072,4093]
+    workload."""
+    run_resid_t(2, 1032, 1799, 714)
+    run_resid_t(2, 1032, 1799, 715, inplace=True)
+    run_resid_t(1, 136, 129, 716, inplace=True)
+    run_resid_t(1, 3072, 4093, 717)
