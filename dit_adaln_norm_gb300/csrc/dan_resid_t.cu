@@ -25,10 +25,11 @@
 // them, and regrouped into token pairs with byte permutes before the add.
 //
 // Other T (residual rows not 16-byte aligned): one 64-channel tile per
-// CTA, each row parity on the 64 tokens whose pairs are 4-byte aligned; the
-// products are formed on the update's channel pairs and stored transposed
-// in shared memory, so the lanes of a warp take consecutive whole token
-// pairs with one aligned shared load each.
+// CTA, each row parity on the 64 tokens whose pairs are 4-byte aligned.  The
+// residual rows are staged in shared memory as 16-byte-aligned windows by
+// cp.async, the products are formed on the update's channel pairs and
+// stored transposed in shared memory, so the lanes of a warp take
+// consecutive whole token pairs with one aligned shared load of each.
 #include "dan_device.cuh"
 #include "dan_internal.h"
 #include "dan_ring.cuh"
@@ -48,6 +49,7 @@ struct ResidParams {
     uint16_t *r_out;
     int64_t T, D, vs;
     unsigned tiles_t, tiles_d, tiles; // tile counts (checked on the host to fit 32 bits)
+    int64_t n16;                      // 16-byte chunks of r (B*D*T*2 is a multiple of 16)
 };
 
 // (a, b) -> the 16-bit halves: low of both, high of both.
@@ -79,14 +81,22 @@ __device__ __forceinline__ TileAt tile_at(const ResidParams &p, unsigned i)
 // layout (channel pairs of one token), and the products bf16(gate * h) are
 // stored transposed in shared memory, one row of 64 tokens per channel in
 // that channel's token range, so lane k's pair is word k of the row
-// (conflict-free).  A warp walks channel rows w, w+4, ... (all of one
-// parity); the residual words are loaded first, so they are in flight with
-// the update tile.
+// (conflict-free).  The residual is read as 16-byte-aligned windows: for
+// each channel row, the chunks from the 16-byte boundary at or before its
+// segment through the segment's end (nine at most), copied by cp.async into
+// shared memory before the update is loaded, so both are in flight
+// together; a warp access of 4-byte words that starts off a sector boundary
+// ran at about half the speed (measured).  A warp then walks channel rows
+// w, w+4, ... (all of one parity): lane k takes its pair from the row's
+// window (one aligned shared load, conflict-free) and its products from
+// word k of the product row, and stores the pair.
 __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_kernel(const ResidParams p)
 {
     constexpr int kPitchW = kTile / 2 + 1; // words per product row (32 used)
     constexpr int kRows = kTile / 4;       // channel rows per warp
     __shared__ uint32_t s_p[kTile * kPitchW + 4];
+    constexpr int kWin = 9;                 // 16-byte chunks per residual window
+    __shared__ uint4 s_r[kTile * kWin];     // residual windows, one per channel row
     uint16_t *s_p16 = reinterpret_cast<uint16_t *>(s_p);
     // First word of channel ch's product row; the upper 32 rows move by four
     // banks, so the eight channel octets of a transposing store hit eight
@@ -108,17 +118,20 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
     const int64_t rstep = 4 * T;   // elements between two rows of a warp
     const int64_t base = ((int64_t)at.b * D + at.d0 + warp) * T + t0 + e; // r[b][d0 + warp][t0 + e]
 
-    uint32_t rw[kRows];
+    // Residual windows: row dl's segment starts at element seg (tokens
+    // t0 - parity ..; seg >= 0, since an odd row is never row 0) and its
+    // window at chunk seg / 8.  B*D*T*2 is a multiple of 16, so a chunk that
+    // starts inside the tensor ends inside it.
     {
-        const uint16_t *q = p.r + base;
 #pragma unroll
-        for (int j = 0; j < kRows; ++j, q += rstep) {
-            rw[j] = 0u;
-            if (warp + 4 * j >= nd) continue; // warp-uniform
-            if (lo_ok && hi_ok) rw[j] = *reinterpret_cast<const uint32_t *>(q);
-            else if (lo_ok) rw[j] = q[0];
-            else if (hi_ok) rw[j] = (uint32_t)q[1] << 16;
+        for (int k = tid; k < kTile * kWin; k += kResidThreads) {
+            const int dl = k / kWin, ch = k - dl * kWin;
+            if (dl >= nd) continue;
+            const int64_t seg = ((int64_t)at.b * D + at.d0 + dl) * T + t0 - (dl & todd); // >= 0, even
+            const int64_t c16 = (seg >> 3) + ch;
+            if (c16 < p.n16) cp_async16(s_r + dl * kWin + ch, p.r + c16 * 8);
         }
+        cp_async_commit();
     }
 
     // Products: thread (channel octet c, update rows tid/8 + 16m), update row
@@ -156,14 +169,19 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
             }
         }
     }
+    cp_async_wait_all(); // this thread's window chunks; the barrier publishes everyone's
     __syncthreads();
 
     uint16_t *q = p.r_out + base;
+    const uint32_t *s_r32 = reinterpret_cast<const uint32_t *>(s_r);
+    int64_t seg = base - 2 * lane; // segment start of this warp's first row: row start + t0 - odd
 #pragma unroll
-    for (int j = 0; j < kRows; ++j, q += rstep) {
+    for (int j = 0; j < kRows; ++j, q += rstep, seg += rstep) {
         const int dl = warp + 4 * j;
         if (dl >= nd) break; // warp-uniform
-        const uint32_t v = hadd2(rw[j], s_p[prow(dl) + lane]);
+        const int mis = (int)(seg & 7); // even: 0, 2, 4 or 6
+        const uint32_t r2 = s_r32[dl * (4 * kWin) + (mis >> 1) + lane]; // tokens t0 + e, + 1
+        const uint32_t v = hadd2(r2, s_p[prow(dl) + lane]);
         if (lo_ok && hi_ok) *reinterpret_cast<uint32_t *>(q) = v;
         else if (lo_ok) q[0] = (uint16_t)v;
         else if (hi_ok) q[1] = (uint16_t)(v >> 16);
@@ -296,6 +314,7 @@ cudaError_t launch_gated_residual_transposed(const ResidProblem &q, cudaStream_t
     p.T = q.T;
     p.D = q.D;
     p.vs = q.vs;
+    p.n16 = q.B * q.D * q.T / 8;
     const int64_t tt = (q.T + kTile - 1) / kTile, td = (q.D + kTile - 1) / kTile;
     if (q.B * tt * td >= (int64_t(1) << 31)) return cudaErrorInvalidValue; // beyond 32-bit tile ids
     p.tiles_t = (unsigned)tt;
