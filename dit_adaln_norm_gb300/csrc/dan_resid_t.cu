@@ -123,13 +123,16 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
     // window at chunk seg / 8.  B*D*T*2 is a multiple of 16, so a chunk that
     // starts inside the tensor ends inside it.
     {
+        // 16 threads per row (the first kWin copy a chunk each), 8 rows per
+        // pass; a thread's rows dl = tid/16 + 8i share one parity
+        const int ch = tid & 15, dl0 = tid >> 4;
+        int64_t seg = ((int64_t)at.b * D + at.d0 + dl0) * T + t0 - (dl0 & todd);
+        const int64_t sstep = 8 * T;
 #pragma unroll
-        for (int k = tid; k < kTile * kWin; k += kResidThreads) {
-            const int dl = k / kWin, ch = k - dl * kWin;
-            if (dl >= nd) continue;
-            const int64_t seg = ((int64_t)at.b * D + at.d0 + dl) * T + t0 - (dl & todd); // >= 0, even
+        for (int i = 0; i < kTile / 8; ++i, seg += sstep) {
+            const int dl = dl0 + 8 * i;
             const int64_t c16 = (seg >> 3) + ch;
-            if (c16 < p.n16) cp_async16(s_r + dl * kWin + ch, p.r + c16 * 8);
+            if (ch < kWin && dl < nd && c16 < p.n16) cp_async16(s_r + dl * kWin + ch, p.r + c16 * 8);
         }
         cp_async_commit();
     }
@@ -143,16 +146,17 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
         if (8 * c < nd) {
             const int64_t dc = (int64_t)at.d0 + 8 * c;
             const uint4 g = ld_vec(reinterpret_cast<const uint4 *>(p.gate + (int64_t)at.b * p.vs + dc));
-            const uint4 *h = p.h + ((int64_t)at.b * T * D + dc) / 8;
             const int64_t tb = t0 - todd;
+            const int64_t hstep = 16 * (D / 8); // 16 update rows
+            const uint4 *h = p.h + (((int64_t)at.b * T + tb + (tid >> 3)) * D + dc) / 8;
             constexpr int kPasses = kTile / 16 + 1;
             uint4 hv[kPasses];
 #pragma unroll
-            for (int m = 0; m < kPasses; ++m) {
+            for (int m = 0; m < kPasses; ++m, h += hstep) {
                 const int hr = (tid >> 3) + 16 * m;
                 const int64_t tk = tb + hr;
                 hv[m] = make_uint4(0, 0, 0, 0);
-                if (hr < kTile + todd && tk >= 0 && tk < T) hv[m] = ld_stream(h + tk * (D / 8));
+                if (hr < kTile + todd && tk >= 0 && tk < T) hv[m] = ld_stream(h);
             }
 #pragma unroll
             for (int m = 0; m < kPasses; ++m) {
@@ -174,13 +178,16 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
 
     uint16_t *q = p.r_out + base;
     const uint32_t *s_r32 = reinterpret_cast<const uint32_t *>(s_r);
-    int64_t seg = base - 2 * lane; // segment start of this warp's first row: row start + t0 - odd
+    // window offset (in words) of this lane's pair: rows of a warp are 4T
+    // elements apart, so the segment's position in its 16-byte chunk
+    // alternates between two values when T is odd and is fixed otherwise
+    const int mis0 = (int)((base - 2 * lane) & 7); // even: 0, 2, 4 or 6
+    const int w0 = (mis0 >> 1) + lane, w1 = ((mis0 ^ (4 * todd)) >> 1) + lane;
 #pragma unroll
-    for (int j = 0; j < kRows; ++j, q += rstep, seg += rstep) {
+    for (int j = 0; j < kRows; ++j, q += rstep) {
         const int dl = warp + 4 * j;
         if (dl >= nd) break; // warp-uniform
-        const int mis = (int)(seg & 7); // even: 0, 2, 4 or 6
-        const uint32_t r2 = s_r32[dl * (4 * kWin) + (mis >> 1) + lane]; // tokens t0 + e, + 1
+        const uint32_t r2 = s_r32[dl * (4 * kWin) + ((j & 1) ? w1 : w0)]; // tokens t0 + e, + 1
         const uint32_t v = hadd2(r2, s_p[prow(dl) + lane]);
         if (lo_ok && hi_ok) *reinterpret_cast<uint32_t *>(q) = v;
         else if (lo_ok) q[0] = (uint16_t)v;
