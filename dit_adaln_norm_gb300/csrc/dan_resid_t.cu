@@ -148,15 +148,17 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
             const uint4 g = ld_vec(reinterpret_cast<const uint4 *>(p.gate + (int64_t)at.b * p.vs + dc));
             const int64_t tb = t0 - todd;
             const int64_t hstep = 16 * (D / 8); // 16 update rows
-            const uint4 *h = p.h + (((int64_t)at.b * T + tb + (tid >> 3)) * D + dc) / 8;
+            // chunk offset of update row tid/8 (may be negative before the
+            // first pass: a pointer is formed only for rows inside the tensor)
+            int64_t hoff = (((int64_t)at.b * T + tb + (tid >> 3)) * D + dc) / 8;
             constexpr int kPasses = kTile / 16 + 1;
             uint4 hv[kPasses];
 #pragma unroll
-            for (int m = 0; m < kPasses; ++m, h += hstep) {
+            for (int m = 0; m < kPasses; ++m, hoff += hstep) {
                 const int hr = (tid >> 3) + 16 * m;
                 const int64_t tk = tb + hr;
                 hv[m] = make_uint4(0, 0, 0, 0);
-                if (hr < kTile + todd && tk >= 0 && tk < T) hv[m] = ld_stream(h);
+                if (hr < kTile + todd && tk >= 0 && tk < T) hv[m] = ld_stream(p.h + hoff);
             }
 #pragma unroll
             for (int m = 0; m < kPasses; ++m) {
