@@ -121,7 +121,10 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
     // Residual windows: row dl's segment starts at element seg (tokens
     // t0 - parity ..; seg >= 0, since an odd row is never row 0) and its
     // window at chunk seg / 8.  B*D*T*2 is a multiple of 16, so a chunk that
-    // starts inside the tensor ends inside it.
+    // starts inside the tensor ends inside it.  The elements of a window
+    // outside its segment belong to neighbouring tiles and are never used,
+    // so in place (r_out == r) their being rewritten by another CTA does not
+    // matter; every element of the segment is read before this CTA writes it.
     {
         // 16 threads per row (the first kWin copy a chunk each), 8 rows per
         // pass; a thread's rows dl = tid/16 + 8i share one parity
