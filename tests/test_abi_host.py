@@ -3,6 +3,7 @@ function include/dan.h declares, and each dan_can_use_* returns the
 documented status.  The pointers here are fake addresses: validation only
 inspects their values, never dereferences them."""
 import ctypes
+import os
 
 import pytest
 
@@ -182,3 +183,12 @@ def test_selftest_argument_checks(lib):
     assert lib.dan_selftest_wait_timeout(0, None) == EINVAL
     assert lib.dan_selftest_wait_timeout(3_000_000_000, None) == EINVAL
     assert lib.dan_get_device_status(None) == EINVAL
+
+
+def test_build_lists_every_source_and_header():
+    """Every CUDA translation unit under csrc/ is compiled into libdan.so, and
+    every header is a dependency of the rebuild check (a file missing from
+    either list would be silently left out of the library or of the check)."""
+    files = os.listdir(dan_build.CSRC)
+    assert sorted(f for f in files if f.endswith(".cu")) == sorted(dan_build.SOURCES)
+    assert sorted(f for f in files if f.endswith((".cuh", ".h"))) == sorted(dan_build.HEADERS)
