@@ -11,14 +11,19 @@ marshals numpy arrays.  bf16 tensors travel as ``np.uint16`` bit patterns.
 Parity status of each function (what pins it is in ``tests/test_oracle_pins.py``):
 
 * ``round_bf16``: pinned (independent nearest-neighbour formulation in fp64).
-* ``rms_modulate`` / ``gated_rms_modulate``: pinned (closed forms, order probes
-  with hand-derived sums, fp64 brute force within 2 bf16 ULP / 1e-6 rstd).
-* ``ln_modulate``: pinned (constant rows, +-a rows, two-chain combine worked by
-  hand, exact 2^k scaling and sign symmetry, fp64 brute force).  The combine's
-  parenthesisation and the cross-warp order are this library's definition:
-  they are fixed by the tests only through the GPU == oracle comparison.
+* ``rms_modulate`` / ``gated_rms_modulate``: pinned (closed forms, +-a rows where
+  eps matters, order probes with hand-derived sums, the weight product order and
+  the division s/D at a width that is not a power of two worked by hand, fp64
+  brute force within 2 bf16 ULP / 1e-6 rstd).
+* ``ln_modulate``: pinned (constant rows, +-a rows, two- and three-chain combines
+  worked by hand, the shfl.down lane and cross-warp orders, the combine's m2
+  count weighting, product order and operand order worked by hand, exact 2^k
+  scaling and sign symmetry, fp64 brute force).  The combine's parenthesisation
+  and the cross-warp order are this library's reading of the pages; the
+  hand-worked rows fix each of them.
 * ``qk_norm_rope_epilogue``: pinned (cos=1/sin=0 and cos=0/sin=1 rotations,
-  V copy, joint order, fp64 brute force); with head_dim 64 and the neox
+  V copy, joint order, the head fold and the weight association worked by
+  hand, eps per stream on small heads, fp64 brute force); with head_dim 64 and the neox
   rotation: the same closed forms, the neox rotation as a column
   permutation of the interleaved one, fp64 brute force.
 * ``gated_ln_modulate``: pinned (r' against an independent elementwise

@@ -297,6 +297,138 @@ def test_qk_head_fold_order_case(hd):
         assert_bits_equal(from_dev(g), w, f"qk fold-order case {name} hd={hd}")
 
 
+# ------------------------------ hand-worked operand-order probes on the GPU
+
+def _golden(name, probe):
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    return {p["name"]: p for p in json.load(open(path))["probes"]}[probe]
+
+
+def _widen(bits):
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32)
+
+
+def test_rms_weight_product_order_probe():
+    """The probe row (tests/golden, rms_weight_product_order: the weight
+    multiplies rn(x*rstd), which puts one column on a bf16 tie) among random
+    rows; GPU == hand-worked values == oracle."""
+    p = _golden("rounding_boundary_probes.json", "rms_weight_product_order")
+    D, T = p["D"], 40
+    x = synth.normal_bf16((1, T, D), 650)
+    probe = synth.to_bf16_bits(np.tile(np.asarray(p["x_alternating"], np.float32), D // 2))
+    x[0, ::7] = probe
+    zero = np.zeros((1, D), np.uint16)
+    w = synth.to_bf16_bits(np.full(D, p["weight"], np.float32))
+    buf, y = guarded((1, T, D))
+    ops.rms_modulate(to_dev(x), to_dev(zero), to_dev(zero), p["eps"], weight=to_dev(w), out=y)
+    torch.cuda.synchronize()
+    check_guard(buf)
+    got = from_dev(y)
+    expect = np.tile(np.asarray(p["expected_y_alternating"], np.float32), D // 2)
+    assert np.array_equal(_widen(got[0, ::7]), np.broadcast_to(expect, got[0, ::7].shape))
+    assert_bits_equal(got, oracle.rms_modulate(x, zero, zero, p["eps"], weight=w), "rms probe")
+
+
+def test_qk_weight_product_order_probe():
+    """Heads of the qk_weight_product_order probe (rn(rn(x*rstd)*w) puts one
+    column on a bf16 tie) at every third Q/K head among random heads, with
+    the identity rotation; GPU == hand-worked values == oracle."""
+    p = _golden("rounding_boundary_probes.json", "qk_weight_product_order")
+    hd, H, Tt, Ti = p["head_dim"], 24, 3, 5
+    pt, pi = synth.packed_qkv(Tt, H, 660, hd), synth.packed_qkv(Ti, H, 661, hd)
+    head = synth.to_bf16_bits(np.tile(np.asarray(p["x_alternating"], np.float32), hd // 2))
+    for arr in (pt, pi):
+        for h in range(0, 2 * H, 3):
+            arr[:, h * hd:(h + 1) * hd] = head
+    ws = [synth.to_bf16_bits(np.full(hd, p["weight"], np.float32))] * 4
+    rope = lambda T: np.concatenate([np.full((T, hd // 2), p["cos"], np.float32),
+                                     np.full((T, hd // 2), p["sin"], np.float32)], 1)
+    Pt, Pi = to_dev(pt), to_dev(pi)
+    outs = ops.qk_norm_rope_epilogue(synth.split_qkv(Pt, H, hd), synth.split_qkv(Pi, H, hd),
+                                     *[to_dev(w) for w in ws], torch.from_numpy(rope(Tt)).cuda(),
+                                     torch.from_numpy(rope(Ti)).cuda(), p["eps"], p["eps"], H,
+                                     head_dim=hd)
+    got = [from_dev(g) for g in outs]
+    expect = np.tile(np.asarray(p["expected_alternating"], np.float32), hd // 2)
+    for h in range(0, 2 * H, 3):
+        src = got[0] if h < H else got[1]
+        assert np.array_equal(_widen(src[:, h % H]), np.broadcast_to(expect, (Tt + Ti, hd)))
+    want = oracle.qk_norm_rope_epilogue(synth.split_qkv(pt, H, hd), synth.split_qkv(pi, H, hd),
+                                        H, ws, rope(Tt), rope(Ti), p["eps"], p["eps"],
+                                        head_dim=hd)
+    for name, g, w in zip("qkv", got, want):
+        assert_bits_equal(g, w, f"qk weight-order probe {name}")
+
+
+def test_ln_combine_count_weighting_probe():
+    """The combine_count_weighting probe row (D = 40: states of 24 and 16
+    elements merge; the count weighting decides one bf16 step of the x = 2
+    outputs at this eps) among random rows; GPU == hand-worked == oracle."""
+    p = _golden("ln_order_probes.json", "combine_count_weighting")
+    D, T = p["D"], 50
+    x = synth.normal_bf16((1, T, D), 670)
+    runs = lambda rr: np.concatenate([np.full(n, v, np.float32) for v, n in rr])
+    x[0, ::5] = synth.to_bf16_bits(runs(p["x_runs"]))
+    zero = np.zeros((1, D), np.uint16)
+    buf, y = guarded((1, T, D))
+    ops.ln_modulate(to_dev(x), to_dev(zero), to_dev(zero), p["eps"], out=y)
+    torch.cuda.synchronize()
+    check_guard(buf)
+    got = from_dev(y)
+    expect = runs([(v, n) for v, (_, n) in zip(p["expected_y_runs"], p["x_runs"])])
+    assert np.array_equal(_widen(got[0, ::5]), np.broadcast_to(expect, got[0, ::5].shape))
+    assert_bits_equal(got, oracle.ln_modulate(x, zero, zero, p["eps"]), "ln combine probe")
+
+
+def _probes(name):
+    import json
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    return json.load(open(path))["probes"]
+
+
+@pytest.mark.parametrize("probe", [p["name"] for p in _probes("ln_order_probes.json")])
+def test_ln_order_probe_rows(probe):
+    """Every hand-worked LayerNorm order probe row among random rows at its
+    own width and eps: GPU == oracle bit for bit."""
+    p = _golden("ln_order_probes.json", probe)
+    D, T = p["D"], 20
+    runs = lambda rr: np.concatenate([np.full(n, v, np.float32) for v, n in rr])
+    row = np.asarray(p["x"], np.float32) if "x" in p else runs(p["x_runs"])
+    x = synth.normal_bf16((1, T, D), 680)
+    x[0, 1::6] = synth.to_bf16_bits(row)
+    zero = np.zeros((1, D), np.uint16)
+    y = torch.empty((1, T, D), dtype=torch.bfloat16, device="cuda")
+    ops.ln_modulate(to_dev(x), to_dev(zero), to_dev(zero), p["eps"], out=y)
+    torch.cuda.synchronize()
+    assert_bits_equal(from_dev(y), oracle.ln_modulate(x, zero, zero, p["eps"]), probe)
+
+
+@pytest.mark.parametrize("probe", [p["name"] for p in _probes("rms_order_probes.json")])
+def test_rms_order_probe_rows(probe):
+    """Every hand-worked RMS order probe row among random rows: GPU == oracle."""
+    p = _golden("rms_order_probes.json", probe)
+    D, T = p["D"], 20
+    row = np.zeros(D, np.float32)
+    cols = p["columns"]
+    if "ones_thread" in cols:
+        tpr = D // 64
+        for b in range(8):
+            row[8 * tpr * b + 8 * cols["ones_thread"]:][:8] = 1.0
+    for c, val in cols["big"]:
+        row[c] = val
+    x = synth.normal_bf16((1, T, D), 681)
+    x[0, 2::5] = synth.to_bf16_bits(row)
+    zero = np.zeros((1, D), np.uint16)
+    eps = p.get("eps", EPS)
+    y = torch.empty((1, T, D), dtype=torch.bfloat16, device="cuda")
+    ops.rms_modulate(to_dev(x), to_dev(zero), to_dev(zero), eps, out=y)
+    torch.cuda.synchronize()
+    assert_bits_equal(from_dev(y), oracle.rms_modulate(x, zero, zero, eps), probe)
+
+
 @pytest.mark.parametrize("H", [24, 3, 1, 30])
 @pytest.mark.parametrize("packed", [True, False])
 def test_qk_small(H, packed):

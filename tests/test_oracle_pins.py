@@ -115,7 +115,8 @@ def _probe_row(p):
 
 
 @pytest.mark.parametrize("name", ["chain_v_fastest", "adjacent_pair_tree",
-                                  "three_warps_padded_tree", "four_warps_tree"])
+                                  "three_warps_padded_tree", "four_warps_tree",
+                                  "non_power_of_two_width"])
 def test_rms_order_probes(orc, name):
     probes = {p["name"]: p for p in json.load(open(os.path.join(GOLDEN,
                                                                 "rms_order_probes.json")))["probes"]}
@@ -123,8 +124,10 @@ def test_rms_order_probes(orc, name):
     D = p["D"]
     x = bits_of(_probe_row(p))[None, None, :]
     zeros = vec(1, D, 0.0)
-    _, st = orc.rms_modulate(x, zeros, zeros, EPS, with_stats=True)
+    _, st = orc.rms_modulate(x, zeros, zeros, p.get("eps", EPS), with_stats=True)
     assert st[0, 0] == np.float32(p["expected_s"]), (st[0, 0], p["expected_s"])
+    if "expected_rstd" in p:
+        assert st[0, 1] == np.float32(p["expected_rstd"]), (st[0, 1], p["expected_rstd"])
 
 
 @pytest.mark.parametrize("D", [2048, 4096, 6144, 8192])
@@ -139,8 +142,10 @@ def test_rms_unit_magnitude_row(orc, D):
     assert np.array_equal(widen(y[0]), sgn.astype(np.float32))
 
 
-@pytest.mark.parametrize("a", [0.5, 1.5, 3.0, 96.0])
+@pytest.mark.parametrize("a", [0.5, 1.5, 3.0, 96.0, 2.0 ** -10])
 def test_rms_alternating_closed_form(orc, a):
+    """+-a row: y = +-1/sqrt(1 + eps/a^2) within one bf16 ULP; at a = 2^-10,
+    a^2 is about eps, so eps moves y by a third."""
     D = 4096
     x = bits_of(a * (-1.0) ** np.arange(D))[None, None]
     zeros = vec(1, D, 0.0)
@@ -231,10 +236,11 @@ def test_ln_three_chain_count_weights_by_hand(orc):
     assert (st[0, 0], st[0, 1]) == (3.0, 64.0)
 
 
-@pytest.mark.parametrize("a", [1.0, 0.25, 3.0])
+@pytest.mark.parametrize("a", [1.0, 0.25, 3.0, 2.0 ** -10])
 def test_ln_alternating_closed_form(orc, a):
     """+-a alternating row: mean 0, var a^2, y = +-1/sqrt(1 + eps/a^2)
-    within 2 bf16 ULP (Welford rounds from n = 3 on)."""
+    within 2 bf16 ULP (Welford rounds from n = 3 on); at a = 2^-10 the eps
+    term is as large as the variance."""
     D = 3072
     sgn = (-1.0) ** np.arange(D)
     x = bits_of(a * sgn)[None, None]
@@ -382,6 +388,29 @@ def test_qk_unit_head_closed_form(orc):
     assert np.array_equal(widen(k).reshape(-1, W), sgn[:, W:2 * W].astype(np.float32))
 
 
+def test_qk_small_head_eps_per_stream(orc):
+    """A head of +-a with a = 2^-10 (a^2 about eps), weight 1, cos = 1 and
+    sin = 0: q = k = +-1/sqrt(1 + eps_s/a^2) within one bf16 ULP, with the
+    text stream's eps for text tokens and the image stream's for image
+    tokens (the epilogue passes each stream's norm epsilon)."""
+    Tt, Ti, H, a = 2, 3, 2, 2.0 ** -10
+    eps_t, eps_i = 1e-6, 4e-6
+    sgn = np.where(np.random.Generator(np.random.PCG64(62)).random((Tt + Ti, 3 * H * 128)) < 0.5,
+                   -1.0, 1.0)
+    packed = bits_of(a * sgn)
+    ones = [bits_of(np.ones(128))] * 4
+    q, k, _ = orc.qk_norm_rope_epilogue(synth.split_qkv(packed[:Tt], H),
+                                        synth.split_qkv(packed[Tt:], H), H, ones,
+                                        _rope_const(Tt, 1, 0), _rope_const(Ti, 1, 0), eps_t, eps_i)
+    W = H * 128
+    mag = np.r_[np.full(Tt, 1.0 / np.sqrt(1.0 + eps_t / a ** 2)),
+                np.full(Ti, 1.0 / np.sqrt(1.0 + eps_i / a ** 2))][:, None]
+    for out, cols in ((q, slice(0, W)), (k, slice(W, 2 * W))):
+        expect = sgn[:, cols] * mag
+        err = np.abs(widen(out).reshape(-1, W) - expect)
+        assert np.all(err <= bf16_ulp(expect))
+
+
 def test_qk_v_copy_and_joint_order(orc):
     Tt, Ti, H = 4, 6, 2
     pt, pi, ws = _qk_inputs(Tt, Ti, H, 62)
@@ -429,7 +458,8 @@ def _runs(runs):
     return np.concatenate([np.full(n, v, np.float64) for v, n in runs])
 
 
-@pytest.mark.parametrize("name", ["welford_reciprocal", "lane_tree_down_order", "cross_warp_order"])
+@pytest.mark.parametrize("name", ["welford_reciprocal", "lane_tree_down_order", "cross_warp_order",
+                                  "combine_m2_product_order", "cross_warp_operand_order"])
 def test_ln_order_probes(orc, name):
     p = _golden("ln_order_probes.json")[name]
     xs = np.asarray(p["x"], np.float64) if "x" in p else _runs(p["x_runs"])
@@ -487,6 +517,52 @@ def test_weight_single_rounding_probe(orc):
                          p["eps"], weight=bits_of(np.full(D, p["weight"])))
     expect = np.tile(np.asarray(p["expected_y_alternating"], np.float32), D // 2)
     assert np.array_equal(widen(y[0, 0]), expect)
+
+
+def test_rms_weight_product_order_probe(orc):
+    """rn(rn(x*rstd)*w): rstd multiplies first, then the weight (ERNIE's
+    (bf16)(x*rstd*w) read left to right); rn(x*w)*rstd lands one fp32 ulp
+    below a bf16 midpoint and rounds the other way."""
+    p = _golden("rounding_boundary_probes.json")["rms_weight_product_order"]
+    D = p["D"]
+    x = np.tile(np.asarray(p["x_alternating"], np.float64), D // 2)
+    y = orc.rms_modulate(bits_of(x)[None, None], vec(1, D, p["scale"]), vec(1, D, p["shift"]),
+                         p["eps"], weight=bits_of(np.full(D, p["weight"])))
+    expect = np.tile(np.asarray(p["expected_y_alternating"], np.float32), D // 2)
+    assert np.array_equal(widen(y[0, 0]), expect)
+
+
+def test_qk_weight_product_order_probe(orc):
+    """Per-head norm with weight: rn(rn(x*rstd)*w), not x*rn(rstd*w)."""
+    p = _golden("rounding_boundary_probes.json")["qk_weight_product_order"]
+    hd, H = p["head_dim"], 2
+    head = np.tile(np.asarray(p["x_alternating"], np.float32), hd // 2)
+    row = np.tile(head, 3 * H)
+    packed = bits_of(np.stack([row, row]))
+    ws = [bits_of(np.full(hd, p["weight"]))] * 4
+    rope = _rope_const_hd(1, hd, p["cos"], p["sin"])
+    q, k, v = orc.qk_norm_rope_epilogue(
+        synth.split_qkv(packed[:1], H, hd), synth.split_qkv(packed[1:], H, hd), H, ws, rope,
+        rope, p["eps"], p["eps"], head_dim=hd)
+    expect = np.tile(np.asarray(p["expected_alternating"], np.float32), hd // 2)
+    for out in (q, k):
+        assert np.array_equal(widen(out).reshape(-1, hd), np.broadcast_to(expect, (2 * H, hd)))
+    assert np.array_equal(v.reshape(2, -1), packed[:, 2 * H * hd:])
+
+
+def test_ln_combine_count_weighting_probe(orc):
+    """The combine's m2 term is rn(rn(rn(delta^2)*nA)*rn(nB/n)) (A the lower
+    state): at counts 24 and 16 the other weighting changes m2 by one ulp,
+    and at this eps the x = 2 outputs by one bf16 step."""
+    p = _golden("ln_order_probes.json")["combine_count_weighting"]
+    D = p["D"]
+    xs = _runs(p["x_runs"])
+    zeros = vec(1, D, 0.0)
+    y, st = orc.ln_modulate(bits_of(xs)[None, None], zeros, zeros, p["eps"], with_stats=True)
+    assert st[0, 0] == np.float32(p["expected_mean"]), float(st[0, 0])
+    assert st[0, 1] == np.float32(p["expected_m2"]), float(st[0, 1])
+    expect = _runs([(v, n) for v, (_, n) in zip(p["expected_y_runs"], p["x_runs"])])
+    assert np.array_equal(widen(y[0, 0]), expect.astype(np.float32))
 
 
 # ------------------------------------- LayerNorm + modulate + static FP8
