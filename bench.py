@@ -178,6 +178,9 @@ class DeviceSet:
 
 NSETS = 4
 KERNELS = ["ln_modulate", "rms_modulate", "gated_rms_modulate", "qk_norm_rope_epilogue"]
+KERNEL_WORKLOADS = {"ln_modulate": "[1,4216,4096] bf16", "rms_modulate": "[1,4216,4096] bf16",
+                    "gated_rms_modulate": "[1,4216,4096] bf16",
+                    "qk_norm_rope_epilogue": "256+4096 tokens x 24 heads x 128 bf16"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -585,6 +588,23 @@ def run_ours(args, rank, world, dist):
     dom = max(KERNELS, key=lambda n: per_kernel[n]["us_per_launch"])
     pk = per_kernel[dom]
     traffic = load_traffic(dom)
+    # every kernel of the step beside the dominant one (the metric names the
+    # ln and rms kernels at the step's shape), and every configuration's
+    # fraction of peak; the full configuration table goes to a side file
+    step_kernels = {n: {"workload": KERNEL_WORKLOADS[n], "us": round(v["us_per_launch"], 3),
+                        "achieved": round(v["gbs"], 1), "frac": round(v["gbs"] / peak, 4),
+                        "traffic": load_traffic(n)}
+                    for n, v in per_kernel.items()}
+    configs_frac = None
+    if configs is not None:
+        configs_frac = {n: round(v["gbs"] / peak, 3) for n, v in configs.items()}
+        table = {n: dict(v, hbm_frac=v["gbs"] / peak) for n, v in configs.items()}
+        if args.configs_out:
+            with open(args.configs_out, "w") as fh:
+                json.dump({"peak_gbs": peak, "configs": table}, fh, indent=1)
+        for n, v in table.items():
+            print(f"config {n}: {v['us_per_launch']:.2f} us, {v['gbs']:.0f} GB/s, "
+                  f"{v['hbm_frac']:.3f} of peak", file=sys.stderr)
     line = {
         "metric": METRIC, "value": agg["gbs"], "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": agg["ms_per_step"],
@@ -598,14 +618,12 @@ def run_ours(args, rank, world, dist):
                             "launches, one step per buffer set); each launch may start while "
                             "the previous kernel drains (programmatic dependent launch)"},
         "hbm_frac": agg["gbs"] / world / peak, "rows_per_s": agg["rows_per_s"],
-        "kernels": {n: dict(v, hbm_frac=v["gbs"] / peak) for n, v in per_kernel.items()},
-        "configs": ({n: dict(v, hbm_frac=v["gbs"] / peak) for n, v in configs.items()}
-                    if configs is not None else None),
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": pk["gbs"], "peak": peak,
                      "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback",
                      "unit": "GB/s", "frac": pk["gbs"] / peak,
-                     "traffic": traffic},
+                     "traffic": traffic, "per_kernel": step_kernels,
+                     "configs_frac": configs_frac},
         "gpu_launches": len(KERNELS) * args.steps,
         "clocks": clock_info,
     }
@@ -815,6 +833,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs-out", default="bench_configs.json",
+                    help="file for the full per-configuration table ('' for none)")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-configuration kernel timings")
     ap.add_argument("--config-launches", type=int, default=0,

@@ -284,47 +284,41 @@ __device__ unsigned int g_device_status;
 
 unsigned *device_status()
 {
-    static unsigned *cache[64] = {nullptr};
+    static DeviceCache<unsigned *> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-    unsigned *&c = cache[dev & 63];
-    if (c == nullptr) {
+    return cached_per_device(cache, dev, []() -> unsigned * {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
-        c = static_cast<unsigned *>(ptr);
-    }
-    return c;
+        return static_cast<unsigned *>(ptr);
+    });
 }
 
 int sm_count()
 {
-    static int cache[64] = {0};
+    static DeviceCache<int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-    const int slot = dev & 63;
-    if (cache[slot] == 0) {
+    return cached_per_device(cache, dev, [dev]() {
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
             n = 1;
-        cache[slot] = n;
-    }
-    return cache[slot];
+        return n;
+    });
 }
 
 int max_smem_optin()
 {
-    static int cache[64] = {0};
+    static DeviceCache<int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-    int &c = cache[dev & 63];
-    if (c == 0) {
+    return cached_per_device(cache, dev, [dev]() {
         int v = 0;
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
             v <= 0)
             v = 48 * 1024;
-        c = v;
-    }
-    return c;
+        return v;
+    });
 }
 
 cudaError_t allow_dynamic_smem(const void *fn, int smem)

@@ -4,7 +4,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace dan {
+
+// Per-device caches of values that never change once known (an SM count,
+// a device symbol's address).  Entries are atomics: host threads that race
+// on a device's first use each compute the same value and store it.
+// Devices beyond the table are served uncached.
+constexpr int kCachedDevices = 64;
+
+template <typename T>
+using DeviceCache = std::atomic<T>[kCachedDevices];
+
+// cache[dev], computing it with compute() the first time; a result equal to
+// T{} (a failed lookup) is returned but not cached.
+template <typename T, typename F>
+T cached_per_device(DeviceCache<T> &cache, int dev, F compute)
+{
+    if (dev < 0 || dev >= kCachedDevices) return compute();
+    T v = cache[dev].load(std::memory_order_relaxed);
+    if (v == T{}) {
+        v = compute();
+        if (v != T{}) cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
 
 // One row problem: [B, T, D] rows, per-batch vectors with batch stride vs
 // (elements), optional weight [D].  Arguments are validated by the shim.

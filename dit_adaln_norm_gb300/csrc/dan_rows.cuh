@@ -847,17 +847,27 @@ int ring_smem(const RowProblem &q, RowParams &p)
     return (int)(fixed + (p.Bs ? vec_bytes : 0));
 }
 
-// One CTA per SM (the slots and the warps' registers fill it), at most one
-// per row; each CTA takes a contiguous block of rows.  `cta_status` is the
-// per-CTA failure record array of CTA_STATUS kernels (nullptr otherwise).
+// CTAs of a row launch: one per SM (the slots and the warps' registers fill
+// it), at most one per row.
+inline int ring_grid(int64_t rows)
+{
+    return (int)(rows < sm_count() ? rows : sm_count());
+}
+
+// Each CTA takes a contiguous block of rows.  CTA_STATUS kernels write one
+// failure record per CTA into `cta_status`, which holds `cta_capacity`
+// records: a launch that would need more is refused (nothing launched).
 template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false>
-cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr)
+cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr,
+                        int cta_capacity = 0)
 {
     RowParams p = make_params(q);
     p.cta_status = cta_status;
     const bool has_w = (KIND == kRms || KIND == kGated) && q.weight != nullptr;
     const int smem = ring_smem<KIND, NW, TW, SPC>(q, p);
-    const int grid = (int)(p.rows < sm_count() ? p.rows : sm_count());
+    const int grid = ring_grid(p.rows);
+    if (CTA_STATUS && (cta_status == nullptr || grid > cta_capacity))
+        return cudaErrorInvalidConfiguration;
     const InvTable2 inv = inv_table();
     auto go = [&](auto fn) -> cudaError_t {
         const cudaError_t e = allow_smem(fn, smem);
@@ -881,6 +891,30 @@ constexpr int kManyRowsPerSm = 24;
 inline bool many_rows(const RowProblem &q)
 {
     return q.B * q.T >= (int64_t)kManyRowsPerSm * sm_count();
+}
+
+// RMSNorm + modulate shapes (warps NW, warps per row TW, slots per team SPC)
+// per width, chosen by measurement: single-warp teams with two slots each,
+// twelve of them when there are many rows per SM and eight otherwise, did
+// better than fewer teams with more slots or multi-warp teams at these
+// widths; rows of 6144 and 8192 are shared by three and four warps, which
+// keeps them in registers.  CTA_STATUS selects the kernels that also write
+// per-CTA failure records (see launch_ring).
+template <bool CTA_STATUS>
+cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr,
+                              int cta_capacity = 0)
+{
+    constexpr bool CS = CTA_STATUS;
+    switch (q.D) {
+    case 2048: return launch_ring<kRms, 1, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
+    case 4096:
+        return many_rows(q)
+                   ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS>(q, s, cta_status, cta_capacity)
+                   : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
+    case 6144: return launch_ring<kRms, 3, 8, 12, 3, 2, false, CS>(q, s, cta_status, cta_capacity);
+    default: // 8192: 4 warps per row
+        return launch_ring<kRms, 4, 8, 16, 4, 1, false, CS>(q, s, cta_status, cta_capacity);
+    }
 }
 
 template <int KIND, bool RAGGED>

@@ -130,10 +130,11 @@ int dan_can_use_rms_modulate(const dan_bf16 *x, const dan_bf16 *weight, const da
  * pool that must not see foreign cudaMalloc/cudaFree).  The pages have no
  * counterpart; it is the same kernel and result as dan_rms_modulate (same
  * arguments, validation and output bits).  Its scratch -- one bounded-wait
- * failure record per CTA, in addition to the device status word -- lives in
- * a static device array of 256 records (1 KB) that the library holds on
- * every GPU that loads it until the process exits; no device memory is
- * allocated or freed.  The launch uses one CTA per SM (at most the row
+ * failure record per CTA, kept for the library's own use -- lives in a
+ * static device array of 256 records (1 KB) that the library holds on every
+ * GPU that loads it until the process exits; no device memory is allocated
+ * or freed.  The records are not part of the interface: a caller learns of
+ * a failed wait through dan_get_device_status, as for every other call.  The launch uses one CTA per SM (at most the row
  * count); a GPU with more than 256 SMs gets DAN_EUNSUPPORTED.  The first
  * call on a device looks up the array's address (cudaGetSymbolAddress), so
  * make that first call before any stream capture.  Every call shares the
