@@ -310,11 +310,19 @@ __global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkPar
     const int64_t t1 = (int64_t)(blockIdx.x + 1) * p.T_all / G;
     const int n = (int)((t1 - t0) * 3 * p.groups);
 
+    const int units = warp < n ? (n - warp + kQkNW - 1) / kQkNW : 0;
+    if (lane == 0) // L2 prefetch of the first units: they stream while the previous grid drains
+        for (int i = 0; i < kQkSPC && i < units; ++i) {
+            QkUnit U;
+            qk_unit<HD>(U, p, t0, warp + kQkNW * i);
+            prefetch_l2(qk_src<HD>(U, p), (unsigned)qk_heads<HD>(U, p) * (unsigned)(HD * 2));
+            if (U.kind != 2) prefetch_l2(qk_rope_row<HD>(U, p), HD * 4u);
+        }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kQkNW * kQkSPC; ++s) mbar_init(full + s, 1);
         mbar_init_fence();
     }
-    grid_dependency_wait(); // no global access above this line
+    grid_dependency_wait(); // no global read above this line (L2 prefetches only)
     allow_dependents();
     if (threadIdx.x < 4 * S::LPH) { // the weights of a stream with no tokens are never read
         const int v = threadIdx.x / S::LPH, s = v >> 1;
@@ -325,7 +333,6 @@ __global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkPar
 
     uint4 *slots = ring + warp * kQkSPC * S::SLOT;
     uint64_t *bar = full + warp * kQkSPC;
-    const int units = warp < n ? (n - warp + kQkNW - 1) / kQkNW : 0;
     auto request = [&](int i) { // lane 0 only
         QkUnit U;
         qk_unit<HD>(U, p, t0, warp + kQkNW * i);

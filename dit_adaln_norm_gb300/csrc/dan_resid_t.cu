@@ -103,7 +103,31 @@ __global__ void __launch_bounds__(kResidThreads, kResidCtas) gated_residual_t_ke
     // different bank groups.
     auto prow = [](int ch) { return ch * kPitchW + (ch >= kTile / 2 ? 4 : 0); };
 
-    grid_dependency_wait(); // no global access above this line
+    {   // L2 prefetch of the tile (it streams while the previous grid drains):
+        // thread k < 64 the lines of residual row k's segment, thread 64 + k
+        // those of update row t0 - 1 + k (and of row t0 + 63)
+        const TileAt at = tile_at(p, blockIdx.x);
+        const int64_t T = p.T, D = p.D;
+        const int k = threadIdx.x & 63;
+        if (threadIdx.x < 64) {
+            if (at.d0 + k < D) {
+                const int64_t s0 = ((int64_t)at.b * D + at.d0 + k) * T + at.t0;
+                const int64_t a = s0 > 0 ? s0 - 1 : 0, z = s0 + (T - at.t0 < kTile ? T - at.t0 : kTile) - 1;
+                prefetch_l2_line(p.r + a);
+                prefetch_l2_line(p.r + z);
+            }
+        } else {
+            const int nd = (int)(D - at.d0 < kTile ? D - at.d0 : kTile);
+            for (int64_t t = (int64_t)at.t0 - 1 + k; t <= (int64_t)at.t0 + kTile - 1; t += 64)
+                if (t >= 0 && t < T) {
+                    const uint16_t *row = reinterpret_cast<const uint16_t *>(p.h) +
+                                          ((int64_t)at.b * T + t) * D + at.d0;
+                    prefetch_l2_line(row);
+                    prefetch_l2_line(row + nd - 1);
+                }
+        }
+    }
+    grid_dependency_wait(); // no global read above this line (L2 prefetches only)
     allow_dependents();
     const int64_t T = p.T, D = p.D;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -261,11 +285,23 @@ __device__ __forceinline__ void pipe_issue(const ResidParams &p, unsigned i, uin
 __global__ void __launch_bounds__(kPThreads, kPipeCtas) gated_residual_t_pipe_kernel(const ResidParams p)
 {
     extern __shared__ __align__(128) uint4 s_pipe[]; // kStages x (update, residual)
-    grid_dependency_wait(); // no global access above this line
-    allow_dependents();
     const unsigned G = gridDim.x;
     const unsigned first = (unsigned)((uint64_t)blockIdx.x * p.tiles / G);
     const unsigned n = (unsigned)((uint64_t)(blockIdx.x + 1) * p.tiles / G) - first;
+    // L2 prefetch of the first tiles (they stream while the previous grid
+    // drains): thread k takes update row k and residual row k of each tile.
+    for (unsigned i = 0; i < (unsigned)(kStages - 1) && i < n; ++i) {
+        const PipeTile at = pipe_tile(p, first + i);
+        const int k = threadIdx.x;
+        const int64_t T = p.T, D = p.D;
+        const int64_t nd = D - at.d0 < kPD ? D - at.d0 : kPD, nt = T - at.t0 < kPT ? T - at.t0 : kPT;
+        if (k < nt)
+            prefetch_l2(p.h + (((int64_t)at.b * T + at.t0 + k) * D + at.d0) / 8, (unsigned)nd * 2u);
+        if (k < nd)
+            prefetch_l2(p.r + ((int64_t)at.b * D + at.d0 + k) * T + at.t0, (unsigned)nt * 2u);
+    }
+    grid_dependency_wait(); // no global read above this line (L2 prefetches only)
+    allow_dependents();
     auto tile_of = [&](unsigned i) { return first + i; };
     auto stage_h = [&](unsigned i) { return s_pipe + (i % kStages) * (kStageH + kStageR); };
     auto stage_r = [&](unsigned i) { return stage_h(i) + kStageH; };

@@ -106,6 +106,23 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
                  : "memory");
 }
 
+// Hint the L2 to fetch `bytes` (a multiple of 16, 16-byte aligned) of
+// global memory.  It returns nothing to the SM, so it may run before the
+// dependency wait on data the previous grid is still writing: the L2 is the
+// point of coherence, a write reaching a line after (or while) it is filled
+// leaves the written data in it, and every read of the data still happens
+// after the wait.
+__device__ __forceinline__ void prefetch_l2(const void *gmem, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
+// The same hint for the cache line holding one address (no alignment).
+__device__ __forceinline__ void prefetch_l2_line(const void *gmem)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(gmem) : "memory");
+}
+
 // After a warp's generic-proxy reads of a slot, order them before the next
 // bulk copy (async proxy) into it: every reading lane fences, then the warp
 // converges, and lane 0 may issue the refill (measured: without the fence a

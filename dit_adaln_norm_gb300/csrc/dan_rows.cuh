@@ -67,6 +67,7 @@ struct RowParams {
     unsigned *status;            // device status word (bounded-wait failures)
     unsigned long long limit_ns; // bound of every wait
     unsigned *cta_status;        // per-CTA failure records (CTA_STATUS kernels only)
+    int l2_ahead;                // rows ahead of a slot request prefetched into L2 (0: none)
 };
 
 // Per-batch vector fragment f: which = 0 -> bf16(1 + scale), 1 -> shift,
@@ -602,6 +603,27 @@ __global__ void __launch_bounds__(32 * NW, 1)
     const int64_t G = gridDim.x;
     const int64_t r0 = (int64_t)blockIdx.x * p.rows / G;
     const int n = (int)((int64_t)(blockIdx.x + 1) * p.rows / G - r0);
+    const int units = team < n ? (n - team + NT - 1) / NT : 0; // rows of this team
+    const bool leader = r == 0 && lane == 0;
+    // L2 prefetch of the team's row i: the rows of the first SPC rounds
+    // before the dependency wait, so that they stream while the previous
+    // grid drains; with l2_ahead > 0 also row i + SPC + l2_ahead when row
+    // i + SPC is requested into its slot.
+    auto prefetch = [&](int i) { // the team leader only
+        const int64_t row = r0 + team + (int64_t)NT * i;
+        prefetch_l2(p.x + row * F, row_bytes);
+        if (NIN == 2) prefetch_l2(p.h + row * F, row_bytes);
+    };
+    if (leader)
+        for (int i = 0; i < SPC && i < units; ++i) prefetch(i);
+    if (threadIdx.x == 32 && p.Bs > 0) { // the staged vectors, likewise
+        if (HAS_W) prefetch_l2(p.weight, row_bytes);
+        for (int b = 0; b < p.Bs; ++b) {
+            prefetch_l2(p.scale + (int64_t)b * p.vs8, row_bytes);
+            prefetch_l2(p.shift + (int64_t)b * p.vs8, row_bytes);
+            if (NV == 3) prefetch_l2(p.gate + (int64_t)b * p.vs8, row_bytes);
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NT * SPC; ++s) mbar_init(full + s, 1);
@@ -611,7 +633,7 @@ __global__ void __launch_bounds__(32 * NW, 1)
         }
         mbar_init_fence();
     }
-    grid_dependency_wait(); // no global access above this line
+    grid_dependency_wait(); // no global read above this line (L2 prefetches only)
     allow_dependents();
     if (CTA_STATUS && threadIdx.x == 0) p.cta_status[blockIdx.x] = 0u;
     stage_begin<NV, HAS_W>(p, s_w, s_vec);
@@ -619,8 +641,6 @@ __global__ void __launch_bounds__(32 * NW, 1)
 
     uint4 *slots = ring + (int64_t)team * SPC * NIN * F;
     uint64_t *bar = full + team * SPC;
-    const int units = team < n ? (n - team + NT - 1) / NT : 0; // rows of this team
-    const bool leader = r == 0 && lane == 0;
     auto request = [&](int i) { // the team leader only
         const int64_t row = r0 + team + (int64_t)NT * i;
         uint4 *dst = slots + (int64_t)Pipe::slot(i) * NIN * F;
@@ -669,7 +689,10 @@ __global__ void __launch_bounds__(32 * NW, 1)
                 if (r == 0 && !mbar_wait(read_bar + team, (unsigned)i & 1u, p.limit_ns))
                     return false;
             }
-            if (leader && i + SPC < units) request(i + SPC);
+            if (leader && i + SPC < units) {
+                request(i + SPC);
+                if (p.l2_ahead > 0 && i + SPC + p.l2_ahead < units) prefetch(i + SPC + p.l2_ahead);
+            }
             return true;
         };
         // Teams of several warps: publish this warp's results (written to
@@ -784,6 +807,7 @@ namespace {
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull; // 1 s per wait
 constexpr int kStageBudget = 96 * 1024; // most shared memory staged vectors may take
+constexpr int kL2Ahead = 0; // rows ahead of each slot request prefetched into L2
 
 // Raise the dynamic shared-memory limit of `fn` the first time it needs more.
 template <typename K>
@@ -815,6 +839,7 @@ RowParams make_params(const RowProblem &q)
     p.status = device_status();
     p.limit_ns = kWaitLimitNs;
     p.cta_status = nullptr;
+    p.l2_ahead = kL2Ahead;
     return p;
 }
 
