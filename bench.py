@@ -840,12 +840,13 @@ def main():
     ap.add_argument("--config-launches", type=int, default=0,
                     help="only launch every configuration this many times, untimed (for ncu)")
     ap.add_argument("--config-filter", default="",
-                    help="keep only the configurations whose name contains this text")
+                    help="keep only the configurations whose name contains one of these |-separated texts")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.config_filter:
-        CONFIGS[:] = [c for c in CONFIGS if args.config_filter in c[0]]
+        keep = args.config_filter.split("|")
+        CONFIGS[:] = [c for c in CONFIGS if any(k in c[0] for k in keep)]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

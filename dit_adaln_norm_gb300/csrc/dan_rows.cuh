@@ -67,6 +67,7 @@ struct RowParams {
     unsigned *status;            // device status word (bounded-wait failures)
     unsigned long long limit_ns; // bound of every wait
     unsigned *cta_status;        // per-CTA failure records (CTA_STATUS kernels only)
+    int l2_pre;                  // rows per team prefetched into L2 before the dependency wait
     int l2_ahead;                // rows ahead of a slot request prefetched into L2 (0: none)
 };
 
@@ -605,17 +606,17 @@ __global__ void __launch_bounds__(32 * NW, 1)
     const int n = (int)((int64_t)(blockIdx.x + 1) * p.rows / G - r0);
     const int units = team < n ? (n - team + NT - 1) / NT : 0; // rows of this team
     const bool leader = r == 0 && lane == 0;
-    // L2 prefetch of the team's row i: the rows of the first SPC rounds
-    // before the dependency wait, so that they stream while the previous
-    // grid drains; with l2_ahead > 0 also row i + SPC + l2_ahead when row
-    // i + SPC is requested into its slot.
+    // L2 prefetch of the team's row i: its first l2_pre rows before the
+    // dependency wait, so that they stream while the previous grid drains;
+    // with l2_ahead > 0 also row i + SPC + l2_ahead when row i + SPC is
+    // requested into its slot.
     auto prefetch = [&](int i) { // the team leader only
         const int64_t row = r0 + team + (int64_t)NT * i;
         prefetch_l2(p.x + row * F, row_bytes);
         if (NIN == 2) prefetch_l2(p.h + row * F, row_bytes);
     };
     if (leader)
-        for (int i = 0; i < SPC && i < units; ++i) prefetch(i);
+        for (int i = 0; i < p.l2_pre && i < units; ++i) prefetch(i);
     if (threadIdx.x == 32 && p.Bs > 0) { // the staged vectors, likewise
         if (HAS_W) prefetch_l2(p.weight, row_bytes);
         for (int b = 0; b < p.Bs; ++b) {
@@ -839,6 +840,7 @@ RowParams make_params(const RowProblem &q)
     p.status = device_status();
     p.limit_ns = kWaitLimitNs;
     p.cta_status = nullptr;
+    p.l2_pre = 0;
     p.l2_ahead = kL2Ahead;
     return p;
 }
@@ -879,15 +881,19 @@ inline int ring_grid(int64_t rows)
     return (int)(rows < sm_count() ? rows : sm_count());
 }
 
-// Each CTA takes a contiguous block of rows.  CTA_STATUS kernels write one
-// failure record per CTA into `cta_status`, which holds `cta_capacity`
-// records: a launch that would need more is refused (nothing launched).
-template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false>
+// Each CTA takes a contiguous block of rows.  Each team prefetches its
+// first PRE rows (SPC when PRE is 0) into L2 before the dependency wait.
+// CTA_STATUS kernels write one failure record per CTA into `cta_status`,
+// which holds `cta_capacity` records: a launch that would need more is
+// refused (nothing launched).
+template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false,
+          int PRE = 0>
 cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr,
                         int cta_capacity = 0)
 {
     RowParams p = make_params(q);
     p.cta_status = cta_status;
+    p.l2_pre = PRE > 0 ? PRE : SPC;
     const bool has_w = (KIND == kRms || KIND == kGated) && q.weight != nullptr;
     const int smem = ring_smem<KIND, NW, TW, SPC>(q, p);
     const int grid = ring_grid(p.rows);
@@ -937,8 +943,8 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
                    ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS>(q, s, cta_status, cta_capacity)
                    : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
     case 6144: return launch_ring<kRms, 3, 8, 12, 3, 2, false, CS>(q, s, cta_status, cta_capacity);
-    default: // 8192: 4 warps per row
-        return launch_ring<kRms, 4, 8, 16, 4, 1, false, CS>(q, s, cta_status, cta_capacity);
+    default: // 8192: 4 warps per row, three rows per team prefetched before the wait
+        return launch_ring<kRms, 4, 8, 16, 4, 1, false, CS, 3>(q, s, cta_status, cta_capacity);
     }
 }
 
@@ -949,9 +955,9 @@ cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
     case 1: return launch_ring<KIND, 4, 1, 8, 1, 1, RAGGED>(q, s);
     case 2: return launch_ring<KIND, 4, 2, 8, 1, 1, RAGGED>(q, s);
     case 3: return many_rows(q) ? launch_ring<KIND, 4, 3, 12, 1, 1, RAGGED>(q, s)
-                                : launch_ring<KIND, 4, 3, 8, 1, 1, RAGGED>(q, s);
+                                : launch_ring<KIND, 4, 3, 16, 2, 1, RAGGED>(q, s);
     case 4: return many_rows(q) ? launch_ring<KIND, 4, 4, 12, 1, 1, RAGGED>(q, s)
-                                : launch_ring<KIND, 4, 4, 8, 1, 1, RAGGED>(q, s);
+                                : launch_ring<KIND, 4, 4, 16, 2, 1, RAGGED>(q, s);
     case 5: return launch_ring<KIND, 4, 5, 8, 2, 2, RAGGED>(q, s);
     case 6: return launch_ring<KIND, 4, 6, 8, 2, 2, RAGGED>(q, s);
     case 7: return launch_ring<KIND, 4, 7, 8, 2, 2, RAGGED>(q, s);

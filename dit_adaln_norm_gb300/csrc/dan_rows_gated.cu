@@ -14,7 +14,8 @@ cudaError_t launch_gated_rms_modulate(const RowProblem &q, cudaStream_t s)
     case 4096: return many_rows(q) ? launch_ring<kGated, 2, 8, 12, 1, 1, false>(q, s)
                                    : launch_ring<kGated, 2, 8, 8, 1, 1, false>(q, s);
     case 6144: return launch_ring<kGated, 3, 8, 6, 3, 1, false>(q, s);
-    default: return launch_ring<kGated, 4, 8, 6, 2, 1, false>(q, s); // 8192: 2 warps per row
+    default: // 8192: 2 warps per row, three rows per team prefetched before the wait
+        return launch_ring<kGated, 4, 8, 6, 2, 1, false, false, 3>(q, s);
     }
 }
 
