@@ -808,7 +808,6 @@ namespace {
 
 constexpr unsigned long long kWaitLimitNs = 1000000000ull; // 1 s per wait
 constexpr int kStageBudget = 96 * 1024; // most shared memory staged vectors may take
-constexpr int kL2Ahead = 0; // rows ahead of each slot request prefetched into L2
 
 // Raise the dynamic shared-memory limit of `fn` the first time it needs more.
 template <typename K>
@@ -841,7 +840,7 @@ RowParams make_params(const RowProblem &q)
     p.limit_ns = kWaitLimitNs;
     p.cta_status = nullptr;
     p.l2_pre = 0;
-    p.l2_ahead = kL2Ahead;
+    p.l2_ahead = 0;
     return p;
 }
 
@@ -882,18 +881,20 @@ inline int ring_grid(int64_t rows)
 }
 
 // Each CTA takes a contiguous block of rows.  Each team prefetches its
-// first PRE rows (SPC when PRE is 0) into L2 before the dependency wait.
+// first PRE rows (SPC when PRE is 0) into L2 before the dependency wait,
+// and with AHEAD > 0 row i + SPC + AHEAD when it requests row i + SPC.
 // CTA_STATUS kernels write one failure record per CTA into `cta_status`,
 // which holds `cta_capacity` records: a launch that would need more is
 // refused (nothing launched).
 template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false,
-          int PRE = 0>
+          int PRE = 0, int AHEAD = 0>
 cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr,
                         int cta_capacity = 0)
 {
     RowParams p = make_params(q);
     p.cta_status = cta_status;
     p.l2_pre = PRE > 0 ? PRE : SPC;
+    p.l2_ahead = AHEAD;
     const bool has_w = (KIND == kRms || KIND == kGated) && q.weight != nullptr;
     const int smem = ring_smem<KIND, NW, TW, SPC>(q, p);
     const int grid = ring_grid(p.rows);
@@ -943,8 +944,9 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
                    ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS>(q, s, cta_status, cta_capacity)
                    : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
     case 6144: return launch_ring<kRms, 3, 8, 12, 3, 2, false, CS>(q, s, cta_status, cta_capacity);
-    default: // 8192: 4 warps per row, three rows per team prefetched before the wait
-        return launch_ring<kRms, 4, 8, 16, 4, 1, false, CS, 3>(q, s, cta_status, cta_capacity);
+    default: // 8192: 4 warps per row; three rows per team prefetched before the
+             // wait, then each row two ahead of the one requested
+        return launch_ring<kRms, 4, 8, 16, 4, 1, false, CS, 3, 1>(q, s, cta_status, cta_capacity);
     }
 }
 
