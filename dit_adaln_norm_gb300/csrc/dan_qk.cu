@@ -41,8 +41,8 @@ struct QkParams {
 
 constexpr int kQkNW = 8;  // warps per CTA (measured best among 4..16)
 constexpr int kQkSPC = 2; // slots per warp (with the first units prefetched into L2 before the
-                          // dependency wait, two measured 0.8-1% faster than one; 6 warps x 2
-                          // and 12 or 16 warps x 1 were slower)
+                          // dependency wait, two beat one; 6 warps x 2 and 12 or 16 warps x 1
+                          // were slower)
 constexpr int kHeadsPerLane = 12; // head fragments a lane holds per unit
 
 // Shape of the work for head_dim HD.
@@ -356,29 +356,15 @@ __global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkPar
     for (int i = 0; i < units; ++i) {
         if (!Pipe::wait(bar, i, p.limit_ns)) {
             Pipe::abort(bar, i, units, p.status, p.limit_ns);
-            if (lane == 0) bulk_wait_all();
             return;
         }
         QkUnit U;
         qk_unit<HD>(U, p, t0, warp + kQkNW * i);
-        const uint4 *slot = slots + Pipe::slot(i) * S::SLOT;
-        if (U.kind == 2) { // V: the heads leave the slot by one bulk store, as they came
-            if (lane == 0) {
-                const int nh = qk_heads<HD>(U, p);
-                bulk_store(p.v_out + (U.tok * p.H + U.h0) * S::LPH, slot, (unsigned)nh * (HD * 2u));
-                bulk_commit();
-                bulk_wait_read<0>(); // the store has read the slot: it may be refilled
-                if (i + kQkSPC < units) request(i + kQkSPC);
-            }
-            __syncwarp();
-            continue;
-        }
-        qk_take<HD, NEOX>(U, p, slot, s_w, hs, fl);
+        qk_take<HD, NEOX>(U, p, slots + Pipe::slot(i) * S::SLOT, s_w, hs, fl);
         slot_reads_done();
         if (lane == 0 && i + kQkSPC < units) request(i + kQkSPC);
         qk_process<HD, NEOX>(U, p, hs, fl);
     }
-    if (lane == 0) bulk_wait_all(); // every V store has completed before the CTA exits
 }
 
 namespace {

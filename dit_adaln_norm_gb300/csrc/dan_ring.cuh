@@ -106,26 +106,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, 
                  : "memory");
 }
 
-// 1-D bulk copy shared -> global of `bytes` (multiple of 16, both addresses
-// 16-byte aligned), in this thread's current bulk group.
-__device__ __forceinline__ void bulk_store(void *gmem_dst, const void *smem_src, unsigned bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
-                 "r"(smem_addr(smem_src)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Hardware waits on this thread's committed bulk store groups: until at most
-// N still read shared memory, and until all of them have completed.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read()
-{
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Hint the L2 to fetch `bytes` (a multiple of 16, 16-byte aligned) of
 // global memory.  It returns nothing to the SM, so it may run before the
 // dependency wait on data the previous grid is still writing: the L2 is the
