@@ -40,6 +40,7 @@ struct QkParams {
 };
 
 constexpr int kQkNW = 8;  // warps per CTA (measured best among 4..16)
+constexpr int kQkPre = 2; // units per warp prefetched into L2 before the dependency wait
 constexpr int kQkSPC = 2; // slots per warp (with the first units prefetched into L2 before the
                           // dependency wait, two beat one; 6 warps x 2 and 12 or 16 warps x 1
                           // were slower)
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(32 * kQkNW, 1) qk_norm_rope_kernel(const QkPar
 
     const int units = warp < n ? (n - warp + kQkNW - 1) / kQkNW : 0;
     if (lane == 0) // L2 prefetch of the first units: they stream while the previous grid drains
-        for (int i = 0; i < kQkSPC && i < units; ++i) {
+        for (int i = 0; i < kQkPre && i < units; ++i) {
             QkUnit U;
             qk_unit<HD>(U, p, t0, warp + kQkNW * i);
             prefetch_l2(qk_src<HD>(U, p), (unsigned)qk_heads<HD>(U, p) * (unsigned)(HD * 2));

@@ -940,8 +940,10 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
     switch (q.D) {
     case 2048: return launch_ring<kRms, 1, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
     case 4096:
+        // one row per team prefetched before the wait (two, one per slot,
+        // measured 11.39 against 10.32 us at [1,4216,4096])
         return many_rows(q)
-                   ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS>(q, s, cta_status, cta_capacity)
+                   ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS, 1>(q, s, cta_status, cta_capacity)
                    : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
     case 6144: return launch_ring<kRms, 3, 8, 12, 3, 2, false, CS>(q, s, cta_status, cta_capacity);
     default: // 8192: 4 warps per row; three rows per team prefetched before the
