@@ -19,6 +19,11 @@
 //    ahead, copies each row from its slot into registers, refills the slot
 //    and computes while the next rows are in flight.  Each row is read
 //    from HBM once.
+//  - Before the dependency wait each team hints its first rows into L2,
+//    so that in back-to-back launches they stream while the previous grid
+//    drains (the CTA starts as soon as the previous grid's CTA on its SM
+//    exits; a prefetch returns nothing to the SM, so it is safe on data the
+//    previous grid still writes).
 //  - The arithmetic of a row depends only on the row's columns, never on
 //    which warp, CTA or launch computes it, so the output bits are
 //    independent of B, T and the grid (batch invariance).
