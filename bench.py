@@ -178,6 +178,8 @@ class DeviceSet:
 
 NSETS = 4
 KERNELS = ["ln_modulate", "rms_modulate", "gated_rms_modulate", "qk_norm_rope_epilogue"]
+E2E_SETS = 2        # device buffer sets the e2e steps rotate through
+E2E_MAX_STEPS = 64  # e2e steps timed (at most; fewer for short runs)
 KERNEL_WORKLOADS = {"ln_modulate": "[1,4216,4096] bf16", "rms_modulate": "[1,4216,4096] bf16",
                     "gated_rms_modulate": "[1,4216,4096] bf16",
                     "qk_norm_rope_epilogue": "256+4096 tokens x 24 heads x 128 bf16"}
@@ -521,26 +523,26 @@ def run_ours(args, rank, world, dist):
 
     # e2e through the public API with pinned host buffers: every step copies
     # its inputs in, runs the 4 launches and copies its outputs back.  Steps
-    # are pipelined over two buffer sets and three streams (copy in, compute,
-    # copy out), so one step's copies overlap its neighbours' work.
+    # are pipelined over E2E_SETS buffer sets and three streams (copy in,
+    # compute, copy out), so one step's copies overlap its neighbours' work.
     e2e = None
     if not args.no_e2e:
-        pipe = sets[:2]
+        pipe = sets[:E2E_SETS]
         h_in = [t.cpu().pin_memory() for t in pipe[0].inputs()]
         h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in s.outputs()]
                  for s in pipe]
         h2d = sum(t.numel() * t.element_size() for t in h_in)
         d2h = sum(t.numel() * t.element_size() for t in h_out[0])
-        e2e_steps = max(4, min(64, args.steps // 20))
+        e2e_steps = max(4, min(E2E_MAX_STEPS, args.steps // 20))
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event()
 
         def e2e_run(n):
             """Issue n pipelined steps; returns the last event of the copy-out stream."""
-            consumed = [None, None]  # compute of the previous step on this set done
-            drained = [None, None]   # copy-out of the previous step on this set done
+            consumed = [None] * len(pipe)  # compute of the previous step on this set done
+            drained = [None] * len(pipe)   # copy-out of the previous step on this set done
             for i in range(n):
-                k = i % 2
+                k = i % len(pipe)
                 s = pipe[k]
                 with torch.cuda.stream(s_in):
                     if consumed[k] is not None:
@@ -564,7 +566,7 @@ def run_ours(args, rank, world, dist):
                     drained[k].record(s_out)
             return drained
 
-        e2e_run(2)
+        e2e_run(len(pipe))
         barrier()
         st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         st.record(s_in)
