@@ -40,10 +40,10 @@ struct QkParams {
 };
 
 constexpr int kQkNW = 8;  // warps per CTA (measured best among 4..16)
-constexpr int kQkPre = 2; // units per warp prefetched into L2 before the dependency wait
-constexpr int kQkSPC = 2; // slots per warp (with the first units prefetched into L2 before the
-                          // dependency wait, two beat one; 6 warps x 2 and 12 or 16 warps x 1
-                          // were slower)
+constexpr int kQkPre = 3; // units per warp prefetched into L2 before the dependency wait
+constexpr int kQkSPC = 3; // slots per warp (with the first units prefetched into L2 before the
+                          // dependency wait: C5 26.02 us with two slots, 25.76 with three;
+                          // 10 or 12 warps x 2 slots were slower)
 constexpr int kHeadsPerLane = 12; // head fragments a lane holds per unit
 
 // Shape of the work for head_dim HD.
