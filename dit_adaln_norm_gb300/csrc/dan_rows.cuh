@@ -577,10 +577,11 @@ struct RowLayout {
 // them in the canonical order, so the result does not depend on TW.  Every
 // wait is bounded.
 // CTA_STATUS kernels also keep one failure record per CTA in
-// p.cta_status[blockIdx.x], cleared when the CTA starts.
+// p.cta_status[blockIdx.x], cleared when the CTA starts.  CPS CTAs share an
+// SM (the register budget is set for that many).
 template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool HAS_W, bool RAGGED,
-          bool STAGED, bool CTA_STATUS = false>
-__global__ void __launch_bounds__(32 * NW, 1)
+          bool STAGED, bool CTA_STATUS = false, int CPS = 1>
+__global__ void __launch_bounds__(32 * NW, CPS)
     row_ring_kernel(const RowParams p, const InvTable2 inv)
 {
     using Shape = RowShape<KIND>;
@@ -862,8 +863,9 @@ InvTable2 inv_table()
 
 // Shared memory a launch of row_ring_kernel<KIND, ..., NW, TW, SPC> needs,
 // with p.Bs set to the number of batches whose vectors are staged (all of
-// them when they fit in the staging budget, else none).
-template <int KIND, int NW, int TW, int SPC>
+// them when they fit in the staging budget, else none).  With CPS CTAs per
+// SM each CTA keeps to its share of the SM's shared memory.
+template <int KIND, int NW, int TW, int SPC, int CPS = 1>
 int ring_smem(const RowProblem &q, RowParams &p)
 {
     using Shape = RowShape<KIND>;
@@ -873,16 +875,18 @@ int ring_smem(const RowProblem &q, RowParams &p)
                           ((KIND == kRms || KIND == kGated) && q.weight ? row_bytes : 0) +
                           Lay::tail_bytes;
     const int64_t vec_bytes = q.B * Shape::NV * row_bytes;
-    const int64_t room = (int64_t)max_smem_optin() - fixed;
+    const int64_t room = (int64_t)max_smem_optin() / CPS - (CPS > 1 ? 2048 : 0) - fixed;
     p.Bs = (vec_bytes <= kStageBudget && vec_bytes <= room) ? (int)q.B : 0;
     return (int)(fixed + (p.Bs ? vec_bytes : 0));
 }
 
-// CTAs of a row launch: one per SM (the slots and the warps' registers fill
-// it), at most one per row.
-inline int ring_grid(int64_t rows)
+// CTAs of a row launch: CPS per SM (one unless the shape is made for
+// several: the slots and the warps' registers fill the SM), at most one per
+// row.
+inline int ring_grid(int64_t rows, int cps = 1)
 {
-    return (int)(rows < sm_count() ? rows : sm_count());
+    const int64_t g = (int64_t)cps * sm_count();
+    return (int)(rows < g ? rows : g);
 }
 
 // Each CTA takes a contiguous block of rows.  Each team prefetches its
@@ -890,9 +894,9 @@ inline int ring_grid(int64_t rows)
 // and with AHEAD > 0 row i + SPC + AHEAD when it requests row i + SPC.
 // CTA_STATUS kernels write one failure record per CTA into `cta_status`,
 // which holds `cta_capacity` records: a launch that would need more is
-// refused (nothing launched).
+// refused (nothing launched).  CPS CTAs share each SM.
 template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false,
-          int PRE = 0, int AHEAD = 0>
+          int PRE = 0, int AHEAD = 0, int CPS = 1>
 cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr,
                         int cta_capacity = 0)
 {
@@ -901,8 +905,8 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
     p.l2_pre = PRE > 0 ? PRE : SPC;
     p.l2_ahead = AHEAD;
     const bool has_w = (KIND == kRms || KIND == kGated) && q.weight != nullptr;
-    const int smem = ring_smem<KIND, NW, TW, SPC>(q, p);
-    const int grid = ring_grid(p.rows);
+    const int smem = ring_smem<KIND, NW, TW, SPC, CPS>(q, p);
+    const int grid = ring_grid(p.rows, CPS);
     if (CTA_STATUS && (cta_status == nullptr || grid > cta_capacity))
         return cudaErrorInvalidConfiguration;
     const InvTable2 inv = inv_table();
@@ -914,11 +918,11 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
     constexpr bool CS = CTA_STATUS;
     if constexpr (KIND == kRms || KIND == kGated) {
         if (has_w)
-            return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, true, CS>)
-                        : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, false, CS>);
+            return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, true, CS, CPS>)
+                        : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, true, RAGGED, false, CS, CPS>);
     }
-    return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, true, CS>)
-                : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, false, CS>);
+    return p.Bs ? go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, true, CS, CPS>)
+                : go(row_ring_kernel<KIND, LW, FPT, NW, TW, SPC, false, RAGGED, false, CS, CPS>);
 }
 
 // Problems with at least this many rows per SM use 12 warps per CTA for the
@@ -957,15 +961,27 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
     }
 }
 
+// LayerNorm shapes (LayerNorm, its FP8 and gated forms) by fragments per
+// logical thread (D / 1024, rounded up).  At D = 3072 and 4096 with many
+// rows: twelve single-warp teams per SM, or for the FP8 producer two CTAs of
+// six (measured 10.82 against 11.10 us at [1,4216,4096], 9.20 against 9.27
+// at [1,4096,3072]); with fewer rows, eight two-warp teams.
+template <int KIND, int FPT, bool RAGGED>
+cudaError_t launch_ln_many(const RowProblem &q, cudaStream_t s)
+{
+    if constexpr (KIND == kLnFp8) return launch_ring<KIND, 4, FPT, 6, 1, 1, RAGGED, false, 0, 0, 2>(q, s);
+    else return launch_ring<KIND, 4, FPT, 12, 1, 1, RAGGED>(q, s);
+}
+
 template <int KIND, bool RAGGED>
 cudaError_t launch_ln_fpt(const RowProblem &q, cudaStream_t s)
 {
     switch ((q.D + 1023) / 1024) {
     case 1: return launch_ring<KIND, 4, 1, 8, 1, 1, RAGGED>(q, s);
     case 2: return launch_ring<KIND, 4, 2, 8, 1, 1, RAGGED>(q, s);
-    case 3: return many_rows(q) ? launch_ring<KIND, 4, 3, 12, 1, 1, RAGGED>(q, s)
+    case 3: return many_rows(q) ? launch_ln_many<KIND, 3, RAGGED>(q, s)
                                 : launch_ring<KIND, 4, 3, 16, 2, 1, RAGGED>(q, s);
-    case 4: return many_rows(q) ? launch_ring<KIND, 4, 4, 12, 1, 1, RAGGED>(q, s)
+    case 4: return many_rows(q) ? launch_ln_many<KIND, 4, RAGGED>(q, s)
                                 : launch_ring<KIND, 4, 4, 16, 2, 1, RAGGED>(q, s);
     case 5: return launch_ring<KIND, 4, 5, 8, 2, 2, RAGGED>(q, s);
     case 6: return launch_ring<KIND, 4, 6, 8, 2, 2, RAGGED>(q, s);
