@@ -12,13 +12,14 @@
 // y to E4M3 with a static scale.
 //
 // Design (HBM-bound row work, no tensor cores):
-//  - One CTA per SM takes a contiguous block of rows.  Its warps form teams
-//    (one to four warps per row); each team requests its own rows with
-//    bulk copies (cp.async.bulk, completion counted on mbarriers, see
-//    dan_ring.cuh) into its own shared-memory slots, one or two rows
-//    ahead, copies each row from its slot into registers, refills the slot
-//    and computes while the next rows are in flight.  Each row is read
-//    from HBM once.
+//  - One CTA per SM (two for one shape) takes a contiguous block of rows or
+//    every G-th row (G CTAs), whichever measured faster for the shape.  Its
+//    warps form teams (one to four warps per row); each team requests its
+//    own rows with bulk copies (cp.async.bulk, completion counted on
+//    mbarriers, see dan_ring.cuh) into its own shared-memory slots, one or
+//    two rows ahead, copies each row from its slot into registers, refills
+//    the slot and computes while the next rows are in flight.  Each row is
+//    read from HBM once.
 //  - Before the dependency wait each team hints its first rows into L2,
 //    so that in back-to-back launches they stream while the previous grid
 //    drains (the CTA starts as soon as the previous grid's CTA on its SM
@@ -74,6 +75,7 @@ struct RowParams {
     unsigned *cta_status;        // per-CTA failure records (CTA_STATUS kernels only)
     int l2_pre;                  // rows per team prefetched into L2 before the dependency wait
     int l2_ahead;                // rows ahead of a slot request prefetched into L2 (0: none)
+    int interleave;              // CTA c takes rows c, c + G, ... (else a contiguous block)
 };
 
 // Per-batch vector fragment f: which = 0 -> bf16(1 + scale), 1 -> shift,
@@ -566,9 +568,10 @@ struct RowLayout {
     static constexpr int tail_bytes = NT * SPC * 8 + 2 * NT * 8 + NT * 2 * kXchFloats * 4;
 };
 
-// CTA c takes the contiguous rows [c*R/G, (c+1)*R/G).  Its warps form
-// NT = NW / TW teams; team t takes the CTA's rows t, t + NT, t + 2NT, ...
-// one at a time and requests each row SPC rows ahead into its own slots
+// CTA c takes the contiguous rows [c*R/G, (c+1)*R/G), or with p.interleave
+// the rows c, c + G, c + 2G, ...  Its warps form NT = NW / TW teams; team t
+// takes the CTA's rows t, t + NT, t + 2NT, ... (in that order of the CTA's
+// rows) one at a time and requests each row SPC rows ahead into its own slots
 // (dan_ring.cuh).  A row's logical warps (LW for RMS, 4 for LayerNorm) are
 // shared among the team's warps, each holding its part in registers.  The
 // leader refills a slot once every warp of the team has read it (team
@@ -608,16 +611,26 @@ __global__ void __launch_bounds__(32 * NW, CPS)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int team = warp / TW, r = warp % TW;
     const int64_t G = gridDim.x;
-    const int64_t r0 = (int64_t)blockIdx.x * p.rows / G;
-    const int n = (int)((int64_t)(blockIdx.x + 1) * p.rows / G - r0);
-    const int units = team < n ? (n - team + NT - 1) / NT : 0; // rows of this team
+    // the team's rows: rbase + rstep * i for i < units
+    int64_t rbase, rstep, rend;
+    if (p.interleave) {
+        rbase = blockIdx.x + G * team;
+        rstep = G * NT;
+        rend = p.rows;
+    } else {
+        const int64_t r0 = (int64_t)blockIdx.x * p.rows / G;
+        rbase = r0 + team;
+        rstep = NT;
+        rend = (int64_t)(blockIdx.x + 1) * p.rows / G;
+    }
+    const int units = rbase < rend ? (int)((rend - rbase + rstep - 1) / rstep) : 0;
     const bool leader = r == 0 && lane == 0;
     // L2 prefetch of the team's row i: its first l2_pre rows before the
     // dependency wait, so that they stream while the previous grid drains;
     // with l2_ahead > 0 also row i + SPC + l2_ahead when row i + SPC is
     // requested into its slot.
     auto prefetch = [&](int i) { // the team leader only
-        const int64_t row = r0 + team + (int64_t)NT * i;
+        const int64_t row = rbase + rstep * i;
         prefetch_l2(p.x + row * F, row_bytes);
         if (NIN == 2) prefetch_l2(p.h + row * F, row_bytes);
     };
@@ -649,7 +662,7 @@ __global__ void __launch_bounds__(32 * NW, CPS)
     uint4 *slots = ring + (int64_t)team * SPC * NIN * F;
     uint64_t *bar = full + team * SPC;
     auto request = [&](int i) { // the team leader only
-        const int64_t row = r0 + team + (int64_t)NT * i;
+        const int64_t row = rbase + rstep * i;
         uint4 *dst = slots + (int64_t)Pipe::slot(i) * NIN * F;
         uint64_t *b = bar + Pipe::slot(i);
         mbar_arrive_expect_tx(b, NIN * row_bytes);
@@ -665,16 +678,20 @@ __global__ void __launch_bounds__(32 * NW, CPS)
         for (int i = 0; i < SPC && i < units; ++i) request(i);
     stage_end<NV>(p, s_vec);
 
-    // Batch of the team's current row, kept incrementally (rows step by NT).
-    int64_t bidx = 0, t_in = 0;
+    // Batch of the team's current row, kept incrementally (rows step by
+    // rstep = q_step * T + r_step).
+    int64_t bidx = 0, t_in = 0, q_step = 0, r_step = 0;
     if (units > 0) {
-        bidx = (r0 + team) / p.T;
-        t_in = (r0 + team) - bidx * p.T;
+        bidx = rbase / p.T;
+        t_in = rbase - bidx * p.T;
+        q_step = rstep / p.T;
+        r_step = rstep - q_step * p.T;
     }
     for (int i = 0; i < units; ++i) {
         if (i > 0) {
-            t_in += NT;
-            while (t_in >= p.T) {
+            bidx += q_step;
+            t_in += r_step;
+            if (t_in >= p.T) {
                 t_in -= p.T;
                 ++bidx;
             }
@@ -684,7 +701,7 @@ __global__ void __launch_bounds__(32 * NW, CPS)
             return;
         }
         const uint4 *src = slots + (int64_t)Pipe::slot(i) * NIN * F;
-        const int64_t row = r0 + team + (int64_t)NT * i;
+        const int64_t row = rbase + rstep * i;
         float *xch = xch_all + (team * 2 + (i & 1)) * kXchFloats;
         // After this warp has read the slot (slot_reads_done): the leader
         // refills it once every warp of the team has read it.  A warp
@@ -847,6 +864,7 @@ RowParams make_params(const RowProblem &q)
     p.cta_status = nullptr;
     p.l2_pre = 0;
     p.l2_ahead = 0;
+    p.interleave = 0;
     return p;
 }
 
@@ -889,14 +907,16 @@ inline int ring_grid(int64_t rows, int cps = 1)
     return (int)(rows < g ? rows : g);
 }
 
-// Each CTA takes a contiguous block of rows.  Each team prefetches its
+// Each CTA takes a contiguous block of rows (or every G-th row with IL).
+// Each team prefetches its
 // first PRE rows (SPC when PRE is 0) into L2 before the dependency wait,
 // and with AHEAD > 0 row i + SPC + AHEAD when it requests row i + SPC.
 // CTA_STATUS kernels write one failure record per CTA into `cta_status`,
 // which holds `cta_capacity` records: a launch that would need more is
-// refused (nothing launched).  CPS CTAs share each SM.
+// refused (nothing launched).  CPS CTAs share each SM.  IL: each CTA takes
+// every G-th row instead of a contiguous block (G CTAs).
 template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false,
-          int PRE = 0, int AHEAD = 0, int CPS = 1>
+          int PRE = 0, int AHEAD = 0, int CPS = 1, bool IL = false>
 cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr,
                         int cta_capacity = 0)
 {
@@ -904,6 +924,7 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
     p.cta_status = cta_status;
     p.l2_pre = PRE > 0 ? PRE : SPC;
     p.l2_ahead = AHEAD;
+    p.interleave = IL ? 1 : 0;
     const bool has_w = (KIND == kRms || KIND == kGated) && q.weight != nullptr;
     const int smem = ring_smem<KIND, NW, TW, SPC, CPS>(q, p);
     const int grid = ring_grid(p.rows, CPS);
@@ -935,7 +956,9 @@ inline bool many_rows(const RowProblem &q)
 }
 
 // RMSNorm + modulate shapes (warps NW, warps per row TW, slots per team SPC)
-// per width, chosen by measurement: single-warp teams with two slots each,
+// per width, each CTA taking every G-th row (measured faster than contiguous
+// blocks at every width: [1,4216,6144] 15.30 against 15.99 us, 8192 20.70
+// against 21.27), chosen by measurement: single-warp teams with two slots each,
 // twelve of them when there are many rows per SM and eight otherwise, did
 // better than fewer teams with more slots or multi-warp teams at these
 // widths; rows of 6144 and 8192 are shared by three and four warps, which
@@ -947,17 +970,20 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
 {
     constexpr bool CS = CTA_STATUS;
     switch (q.D) {
-    case 2048: return launch_ring<kRms, 1, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
+    case 2048:
+        return launch_ring<kRms, 1, 8, 8, 1, 2, false, CS, 0, 0, 1, true>(q, s, cta_status, cta_capacity);
     case 4096:
         // one row per team prefetched before the wait (two, one per slot,
         // measured 11.39 against 10.32 us at [1,4216,4096])
-        return many_rows(q)
-                   ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS, 1>(q, s, cta_status, cta_capacity)
-                   : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS>(q, s, cta_status, cta_capacity);
-    case 6144: return launch_ring<kRms, 3, 8, 12, 3, 2, false, CS>(q, s, cta_status, cta_capacity);
+        return many_rows(q) ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS, 1, 0, 1, true>(
+                                  q, s, cta_status, cta_capacity)
+                            : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS, 0, 0, 1, true>(
+                                  q, s, cta_status, cta_capacity);
+    case 6144:
+        return launch_ring<kRms, 3, 8, 12, 3, 2, false, CS, 0, 0, 1, true>(q, s, cta_status, cta_capacity);
     default: // 8192: 4 warps per row; three rows per team prefetched before the
              // wait, then each row two ahead of the one requested
-        return launch_ring<kRms, 4, 8, 16, 4, 1, false, CS, 3, 1>(q, s, cta_status, cta_capacity);
+        return launch_ring<kRms, 4, 8, 16, 4, 1, false, CS, 3, 1, 1, true>(q, s, cta_status, cta_capacity);
     }
 }
 
@@ -965,11 +991,17 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
 // logical thread (D / 1024, rounded up).  At D = 3072 and 4096 with many
 // rows: twelve single-warp teams per SM, or for the FP8 producer two CTAs of
 // six (measured 10.82 against 11.10 us at [1,4216,4096], 9.20 against 9.27
-// at [1,4096,3072]); with fewer rows, eight two-warp teams.
+// at [1,4096,3072]); with fewer rows, eight two-warp teams.  Every G-th row
+// per CTA (rather than a contiguous block) where that measured faster: the
+// gated form, and LayerNorm at D = 4096 (11.05 against 11.11 us at
+// [1,4216,4096]; at D = 3072 9.05 against 9.00, and slower for the FP8
+// producer and the two-warp teams).
 template <int KIND, int FPT, bool RAGGED>
 cudaError_t launch_ln_many(const RowProblem &q, cudaStream_t s)
 {
     if constexpr (KIND == kLnFp8) return launch_ring<KIND, 4, FPT, 6, 1, 1, RAGGED, false, 0, 0, 2>(q, s);
+    else if constexpr (KIND == kGatedLn || FPT == 4)
+        return launch_ring<KIND, 4, FPT, 12, 1, 1, RAGGED, false, 0, 0, 1, true>(q, s);
     else return launch_ring<KIND, 4, FPT, 12, 1, 1, RAGGED>(q, s);
 }
 
