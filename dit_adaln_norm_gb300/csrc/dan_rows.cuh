@@ -987,22 +987,20 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
     }
 }
 
-// LayerNorm shapes (LayerNorm, its FP8 and gated forms) by fragments per
-// logical thread (D / 1024, rounded up).  At D = 3072 and 4096 with many
-// rows: twelve single-warp teams per SM, or for the FP8 producer two CTAs of
-// six (measured 10.82 against 11.10 us at [1,4216,4096], 9.20 against 9.27
-// at [1,4096,3072]); with fewer rows, eight two-warp teams.  Every G-th row
-// per CTA (rather than a contiguous block) where that measured faster: the
-// gated form, and LayerNorm at D = 4096 (11.05 against 11.11 us at
-// [1,4216,4096]; at D = 3072 9.05 against 9.00, and slower for the FP8
-// producer and the two-warp teams).
+// LayerNorm shapes (LayerNorm and its FP8 form) by fragments per logical
+// thread (D / 1024, rounded up).  At D = 3072 and 4096 with many rows:
+// twelve single-warp teams per SM, each CTA taking every G-th row (against
+// a contiguous block per CTA: 11.05 against 11.11 us at [1,4216,4096],
+// 9.05 against 9.00 and 9.12 against 9.50 us at [1,4096,3072] on two
+// boxes); for the FP8 producer two CTAs of six per SM on contiguous blocks
+// (10.82 against 11.10 us at [1,4216,4096], 9.20 against 9.27 at
+// [1,4096,3072]; interleaved rows measured 0.1 to 0.25 us slower on one box
+// and as much faster on another).  With fewer rows: eight two-warp teams.
 template <int KIND, int FPT, bool RAGGED>
 cudaError_t launch_ln_many(const RowProblem &q, cudaStream_t s)
 {
     if constexpr (KIND == kLnFp8) return launch_ring<KIND, 4, FPT, 6, 1, 1, RAGGED, false, 0, 0, 2>(q, s);
-    else if constexpr (KIND == kGatedLn || FPT == 4)
-        return launch_ring<KIND, 4, FPT, 12, 1, 1, RAGGED, false, 0, 0, 1, true>(q, s);
-    else return launch_ring<KIND, 4, FPT, 12, 1, 1, RAGGED>(q, s);
+    else return launch_ring<KIND, 4, FPT, 12, 1, 1, RAGGED, false, 0, 0, 1, true>(q, s);
 }
 
 template <int KIND, bool RAGGED>

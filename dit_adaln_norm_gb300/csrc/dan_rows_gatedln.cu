@@ -8,16 +8,19 @@ namespace dan {
 namespace {
 
 // A slot holds r and h (twice a LayerNorm slot), so wide rows get fewer
-// slots than the plain LayerNorm.
+// slots than the plain LayerNorm.  With many rows each CTA takes every G-th
+// row (against a contiguous block per CTA: 14.95 against 15.02 and 14.98
+// against 15.30 us at [1,4096,3072], 20.99 against 21.02 and 20.89 against
+// 21.16 at [1,4216,4096], on two boxes).
 template <bool RAGGED>
 cudaError_t launch_gated_ln_fpt(const RowProblem &q, cudaStream_t s)
 {
     switch ((q.D + 1023) / 1024) {
     case 1: return launch_ring<kGatedLn, 4, 1, 8, 1, 1, RAGGED>(q, s);
     case 2: return launch_ring<kGatedLn, 4, 2, 8, 1, 1, RAGGED>(q, s);
-    case 3: return many_rows(q) ? launch_ring<kGatedLn, 4, 3, 12, 1, 1, RAGGED>(q, s)
+    case 3: return many_rows(q) ? launch_ring<kGatedLn, 4, 3, 12, 1, 1, RAGGED, false, 0, 0, 1, true>(q, s)
                                 : launch_ring<kGatedLn, 4, 3, 8, 1, 1, RAGGED>(q, s);
-    case 4: return many_rows(q) ? launch_ring<kGatedLn, 4, 4, 12, 1, 1, RAGGED>(q, s)
+    case 4: return many_rows(q) ? launch_ring<kGatedLn, 4, 4, 12, 1, 1, RAGGED, false, 0, 0, 1, true>(q, s)
                                 : launch_ring<kGatedLn, 4, 4, 8, 1, 1, RAGGED>(q, s);
     case 5: return launch_ring<kGatedLn, 4, 5, 8, 2, 1, RAGGED>(q, s);
     case 6: return launch_ring<kGatedLn, 4, 6, 8, 2, 1, RAGGED>(q, s);
