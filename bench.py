@@ -15,7 +15,8 @@ other traffic passes, above the 129 MB L2) so every kernel reads cold data;
 CUDA events on the launching stream, barrier + synchronize on both sides,
 max over ranks.  Per-kernel launch durations come from separate graph
 loops of each kernel alone.  e2e: the same step with pinned host inputs
-copied in and every output copied back inside the timed region.
+copied in and every output copied back inside the timed region (one copy
+each way per step: a buffer set's tensors are views into one flat buffer).
 
 --impl reference times the CPU oracle (test infrastructure, the reference arm
 of this comparison) on a bounded sample of the same workload.
@@ -120,34 +121,48 @@ class HostInputs:
 
 
 class DeviceSet:
-    """One set of device buffers (inputs + outputs) for a full step."""
+    """One set of device buffers for a full step.  The inputs are views into
+    one flat device buffer and the outputs into another (each view 256-byte
+    aligned), so the e2e step moves each direction with a single copy."""
+
+    ALIGN = 256
 
     def __init__(self, h: HostInputs, dev):
         import torch
-
-        def up(bits):
-            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
-                torch.bfloat16).to(dev)
-
-        self.ln_x, self.ln_emb = up(h.ln_x), up(h.ln_emb)
-        self.rms_x, self.rms_emb = up(h.rms_x), up(h.rms_emb)
-        self.g_r, self.g_h, self.g_emb = up(h.g_r), up(h.g_h), up(h.g_emb)
-        self.qk_txt, self.qk_img = up(h.qk_txt), up(h.qk_img)
-        self.qk_w = up(h.qk_w)
-        self.rope_txt = torch.from_numpy(h.rope_txt).to(dev)
-        self.rope_img = torch.from_numpy(h.rope_img).to(dev)
-        e = lambda t: torch.empty_like(t)
-        self.ln_y, self.rms_y, self.g_rout, self.g_y = e(self.ln_x), e(self.rms_x), e(self.g_r), e(self.g_r)
+        bf16 = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        srcs = [("ln_x", bf16(h.ln_x)), ("ln_emb", bf16(h.ln_emb)), ("rms_x", bf16(h.rms_x)),
+                ("rms_emb", bf16(h.rms_emb)), ("g_r", bf16(h.g_r)), ("g_h", bf16(h.g_h)),
+                ("g_emb", bf16(h.g_emb)), ("qk_txt", bf16(h.qk_txt)), ("qk_img", bf16(h.qk_img)),
+                ("qk_w", bf16(h.qk_w)), ("rope_txt", torch.from_numpy(h.rope_txt)),
+                ("rope_img", torch.from_numpy(h.rope_img))]
+        self.in_buf, views = self._pack([(n, t.shape, t.dtype) for n, t in srcs], dev)
+        for (n, t), v in zip(srcs, views):
+            v.copy_(t)
+            setattr(self, n, v)
         T = T_TXT + T_IMG
-        self.q_out, self.k_out, self.v_out = (torch.empty((T, HEADS, 128), dtype=torch.bfloat16,
-                                                          device=dev) for _ in range(3))
+        row = (1, T_ROWS, D)
+        outs = [("ln_y", row, torch.bfloat16), ("rms_y", row, torch.bfloat16),
+                ("g_rout", row, torch.bfloat16), ("g_y", row, torch.bfloat16)] + \
+               [(n, (T, HEADS, 128), torch.bfloat16) for n in ("q_out", "k_out", "v_out")]
+        self.out_buf, views = self._pack(outs, dev)
+        for (n, _, _), v in zip(outs, views):
+            setattr(self, n, v)
 
-    def inputs(self):
-        return [self.ln_x, self.ln_emb, self.rms_x, self.rms_emb, self.g_r, self.g_h, self.g_emb,
-                self.qk_txt, self.qk_img, self.qk_w, self.rope_txt, self.rope_img]
-
-    def outputs(self):
-        return [self.ln_y, self.rms_y, self.g_rout, self.g_y, self.q_out, self.k_out, self.v_out]
+    @classmethod
+    def _pack(cls, specs, dev):
+        """A flat byte buffer on `dev` and one view per (name, shape, dtype)."""
+        import torch
+        offs, total = [], 0
+        for _, shape, dtype in specs:
+            offs.append(total)
+            nb = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            total += (nb + cls.ALIGN - 1) // cls.ALIGN * cls.ALIGN
+        buf = torch.empty(total, dtype=torch.uint8, device=dev)
+        views = []
+        for (_, shape, dtype), off in zip(specs, offs):
+            nb = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            views.append(buf[off:off + nb].view(dtype).view(shape))
+        return buf, views
 
     def vec(self, emb, i):
         return emb[:, i * D:(i + 1) * D]
@@ -528,11 +543,11 @@ def run_ours(args, rank, world, dist):
     e2e = None
     if not args.no_e2e:
         pipe = sets[:E2E_SETS]
-        h_in = [t.cpu().pin_memory() for t in pipe[0].inputs()]
-        h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in s.outputs()]
-                 for s in pipe]
-        h2d = sum(t.numel() * t.element_size() for t in h_in)
-        d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+        # one pinned host image of a set's inputs, one of its outputs per set
+        h_in = pipe[0].in_buf.cpu().pin_memory()
+        h_out = [torch.empty(s.out_buf.shape, dtype=torch.uint8, pin_memory=True) for s in pipe]
+        h2d = h_in.numel()
+        d2h = h_out[0].numel()
         e2e_steps = max(4, min(E2E_MAX_STEPS, args.steps // 20))
         s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event()
@@ -547,8 +562,7 @@ def run_ours(args, rank, world, dist):
                 with torch.cuda.stream(s_in):
                     if consumed[k] is not None:
                         s_in.wait_event(consumed[k])
-                    for d, hsrc in zip(s.inputs(), h_in):
-                        d.copy_(hsrc, non_blocking=True)
+                    s.in_buf.copy_(h_in, non_blocking=True)
                     loaded = ev()
                     loaded.record(s_in)
                 with torch.cuda.stream(stream):
@@ -560,8 +574,7 @@ def run_ours(args, rank, world, dist):
                     consumed[k].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(consumed[k])
-                    for hdst, d in zip(h_out[k], s.outputs()):
-                        hdst.copy_(d, non_blocking=True)
+                    h_out[k].copy_(s.out_buf, non_blocking=True)
                     drained[k] = ev()
                     drained[k].record(s_out)
             return drained
