@@ -532,6 +532,23 @@ def test_ln_fp8_metric_shape_and_cfg_batch():
     run_ln_fp8(2, 1140, 4096, synth.SEED_X + 1, 0.05)
 
 
+# ------------------------------------- rows of several batches per team
+
+@pytest.mark.parametrize("B,T", [(3, 1300), (5, 777)])
+def test_rows_across_batches(B, T):
+    """Enough rows for the twelve-warp shapes, with fewer tokens per batch
+    than the rows between two of a team's rows in the interleaved order (152
+    CTAs x 12 teams), so a team's batch index advances by one or two batches
+    per row."""
+    run_rms(B, T, 4096, 620 + T)
+    run_rms(B, T, 8192, 621 + T, weight=True)
+    run_gated(B, T, 4096, 622 + T)
+    run_ln(B, T, 4096, 623 + T, outliers=True)
+    run_ln(B, T, 3072, 624 + T)
+    run_ln_fp8(B, T, 4096, 625 + T, 0.05)
+    run_gated_ln(B, T, 3072, 626 + T)
+
+
 # ------------------------------------------------ gated residual + LayerNorm
 
 def run_gated_ln(B, T, D, seed, inplace=False, chunks=6):
