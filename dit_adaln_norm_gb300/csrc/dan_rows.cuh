@@ -992,9 +992,9 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
 // twelve single-warp teams per SM, each CTA taking every G-th row (against
 // a contiguous block per CTA: 11.05 against 11.11 us at [1,4216,4096],
 // 9.05 against 9.00 and 9.12 against 9.50 us at [1,4096,3072] on two
-// boxes); for the FP8 producer two CTAs of six per SM on contiguous blocks
+// GB300s); for the FP8 producer two CTAs of six per SM on contiguous blocks
 // (10.82 against 11.10 us at [1,4216,4096], 9.20 against 9.27 at
-// [1,4096,3072]; interleaved rows measured 0.1 to 0.25 us slower on one box
+// [1,4096,3072]; interleaved rows measured 0.1 to 0.25 us slower on one GB300
 // and as much faster on another).  With fewer rows: eight two-warp teams.
 template <int KIND, int FPT, bool RAGGED>
 cudaError_t launch_ln_many(const RowProblem &q, cudaStream_t s)

@@ -11,7 +11,7 @@ namespace {
 // slots than the plain LayerNorm.  With many rows each CTA takes every G-th
 // row (against a contiguous block per CTA: 14.95 against 15.02 and 14.98
 // against 15.30 us at [1,4096,3072], 20.99 against 21.02 and 20.89 against
-// 21.16 at [1,4216,4096], on two boxes).
+// 21.16 at [1,4216,4096], on two GB300s).
 template <bool RAGGED>
 cudaError_t launch_gated_ln_fpt(const RowProblem &q, cudaStream_t s)
 {
