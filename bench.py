@@ -362,8 +362,8 @@ def _oracle_rate(h: HostInputs, threads: int, budget_s: float):
         total_b += b
         total_r += r
         reps += 1
-    sample = (f"{reps} pass(es) over the first {rows} rows of each [1,4216,4096] row workload "
-              f"and {rows} tokens of the QKV epilogue, rows split over {threads} thread(s)")
+    sample = (f"{reps} passes over the first {rows} rows of each row workload and {rows} "
+              f"QKV tokens, {threads} threads")
     return total_b / total_t / 1e9, total_r / total_t, sample
 
 
@@ -612,7 +612,7 @@ def run_ours(args, rank, world, dist):
                     for n, v in per_kernel.items()}
     configs_frac = None
     if configs is not None:
-        configs_frac = {n: round(v["gbs"] / peak, 3) for n, v in configs.items()}
+        configs_frac = {CONFIG_IDS.get(n, n): round(v["gbs"] / peak, 3) for n, v in configs.items()}
         table = {n: dict(v, hbm_frac=v["gbs"] / peak) for n, v in configs.items()}
         if args.configs_out:
             with open(args.configs_out, "w") as fh:
@@ -627,11 +627,9 @@ def run_ours(args, rank, world, dist):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes()[0],
                    "rows_per_step": step_bytes()[1],
-                   "l2": "inputs rotate over 4 device buffer sets (~1.8 GB); >= 200 MB of "
-                         "other traffic between two uses of a buffer (L2 is 129 MB)",
-                   "graph": "steps replayed from one CUDA graph of 4 consecutive steps (16 "
-                            "launches, one step per buffer set); each launch may start while "
-                            "the previous kernel drains (programmatic dependent launch)"},
+                   "l2": "4 rotating buffer sets (~1.8 GB), >= 200 MB between two uses "
+                         "of a buffer (L2 129 MB)",
+                   "graph": "4-step CUDA graphs, programmatic dependent launch"},
         "hbm_frac": agg["gbs"] / world / peak, "rows_per_s": agg["rows_per_s"],
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": pk["gbs"], "peak": peak,
                      "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)"
@@ -662,6 +660,24 @@ def run_ours(args, rank, world, dist):
 # neox rotation and head_dim 64).  Each is timed alone; these are
 # per-kernel figures, not part of the step.  (name, kind, B, T, D, flag):
 # flag is the RMS weight, or for "qk" the neox rotation with D = head_dim.
+# Short names of the configurations for the JSON line (the full names label
+# the side file and the per-configuration lines on stderr).
+CONFIG_IDS = {
+    "C1 rms [1,128,2048]": "C1", "C1' rms [1,4216,4096]": "C1'", "C2a ln [1,4096,3072]": "C2a",
+    "C2b ln [1,512,3072]": "C2b", "C2c ln [1,4608,3072]": "C2c", "C2d ln [1,4093,3072]": "C2d",
+    "C2' ln [1,4216,4096]": "C2'", "C3 gated [1,4216,4096]": "C3", "C4 ln CFG [2,1140,4096]": "C4",
+    "C5 qk 256+4096 tokens x 24 heads x 128": "C5",
+    "N4 rms+weight [1,4216,6144]": "N4 rms 6144", "N4 rms+weight [1,4216,8192]": "N4 rms 8192",
+    "N4 gated [1,4216,8192]": "N4 gated 8192", "N1 ln+fp8 [1,4216,4096]": "N1 4096",
+    "N1 ln+fp8 [1,4096,3072]": "N1 3072", "N2 gated ln [1,4216,4096]": "N2 gated ln 4096",
+    "N2 gated ln [1,4096,3072]": "N2 gated ln 3072",
+    "N3 qk neox 256+4096 tokens x 24 heads x 128": "N3 neox hd128",
+    "N3 qk 256+4096 tokens x 48 heads x 64": "N3 hd64",
+    "N3 qk neox 256+4096 tokens x 48 heads x 64": "N3 neox hd64",
+    "N2 gated residual, [1,3072,4096] residual layout": "N2 resid T4096",
+    "N2 gated residual, [1,3072,4093] residual layout (odd T)": "N2 resid T4093",
+}
+
 CONFIGS = [
     ("C1 rms [1,128,2048]", "rms", 1, 128, 2048, False),
     ("C1' rms [1,4216,4096]", "rms", 1, 4216, 4096, False),

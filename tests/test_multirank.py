@@ -76,3 +76,13 @@ def test_reference_arm_runs_on_rank_zero_only():
     line = json.loads(r0.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_configuration_ids_cover_every_configuration():
+    """The JSON line keys each configuration's fraction of peak by a short id;
+    every configuration has exactly one, and no two share it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    names = [c[0] for c in bench.CONFIGS]
+    assert sorted(names) == sorted(bench.CONFIG_IDS)
+    assert len(set(bench.CONFIG_IDS.values())) == len(names)
