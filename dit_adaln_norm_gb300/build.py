@@ -6,6 +6,7 @@ FMA contraction anywhere), IEEE division and square root, no flush-to-zero.
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -46,6 +47,16 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     if not force and not _stale():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
+    # processes sharing the tree (the ranks of one job) build one at a time:
+    # the objects have fixed paths; a waiter finds the library fresh
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not _stale():
+            return LIB
+        return _compile(verbose, extra)
+
+
+def _compile(verbose: bool, extra: list[str] | None) -> str:
     cc = nvcc()
     extra = list(extra or [])
     procs = []
