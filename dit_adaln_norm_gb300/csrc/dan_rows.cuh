@@ -76,6 +76,7 @@ struct RowParams {
     int l2_pre;                  // rows per team prefetched into L2 before the dependency wait
     int l2_ahead;                // rows ahead of a slot request prefetched into L2 (0: none)
     int interleave;              // CTA c takes rows c, c + G, ... (else a contiguous block)
+    int l2_pre_skip;             // > 1: teams t with t % l2_pre_skip == l2_pre_skip - 1 skip it
 };
 
 // Per-batch vector fragment f: which = 0 -> bf16(1 + scale), 1 -> shift,
@@ -641,7 +642,10 @@ __global__ void __launch_bounds__(32 * NW, CPS)
         if (NIN == 2) prefetch_l2(p.h + row * F, row_bytes);
     };
     if (leader)
-        for (int i = 0; i < p.l2_pre && i < units; ++i) prefetch(i);
+        for (int i = 0; i < p.l2_pre && i < units; ++i) {
+            if (p.l2_pre_skip > 1 && team % p.l2_pre_skip == p.l2_pre_skip - 1) break;
+            prefetch(i);
+        }
     if (threadIdx.x == 32 && p.Bs > 0) { // the staged vectors, likewise
         if (HAS_W) prefetch_l2(p.weight, row_bytes);
         for (int b = 0; b < p.Bs; ++b) {
@@ -871,6 +875,7 @@ RowParams make_params(const RowProblem &q)
     p.l2_pre = 0;
     p.l2_ahead = 0;
     p.interleave = 0;
+    p.l2_pre_skip = 1;
     return p;
 }
 
@@ -920,9 +925,14 @@ inline int ring_grid(int64_t rows, int cps = 1)
 // CTA_STATUS kernels write one failure record per CTA into `cta_status`,
 // which holds `cta_capacity` records: a launch that would need more is
 // refused (nothing launched).  CPS CTAs share each SM.  IL: each CTA takes
-// every G-th row instead of a contiguous block (G CTAs).
+// every G-th row instead of a contiguous block (G CTAs).  SKIP > 1: every
+// SKIP-th team prefetches nothing before the wait, so the first burst is
+// smaller and lands sooner and those teams' rows follow it (measured faster
+// with SKIP = 3 for every shape measured but RMS at D = 4096: C2' 10.91
+// against 11.34 us, C3 20.36 against 20.83, [1,4216,8192] RMS 20.27
+// against 20.93; C1' 10.44 against 10.27).
 template <int KIND, int LW, int FPT, int NW, int TW, int SPC, bool RAGGED, bool CTA_STATUS = false,
-          int PRE = 0, int AHEAD = 0, int CPS = 1, bool IL = false>
+          int PRE = 0, int AHEAD = 0, int CPS = 1, bool IL = false, int SKIP = 3>
 cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_status = nullptr,
                         int cta_capacity = 0)
 {
@@ -931,6 +941,7 @@ cudaError_t launch_ring(const RowProblem &q, cudaStream_t s, unsigned *cta_statu
     p.l2_pre = PRE > 0 ? PRE : SPC;
     p.l2_ahead = AHEAD;
     p.interleave = IL ? 1 : 0;
+    p.l2_pre_skip = SKIP;
     const bool has_w = (KIND == kRms || KIND == kGated) && q.weight != nullptr;
     const int smem = ring_smem<KIND, NW, TW, SPC, CPS>(q, p);
     const int grid = ring_grid(p.rows, CPS);
@@ -981,9 +992,9 @@ cudaError_t launch_rms_shapes(const RowProblem &q, cudaStream_t s, unsigned *cta
     case 4096:
         // one row per team prefetched before the wait (two, one per slot,
         // measured 11.39 against 10.32 us at [1,4216,4096])
-        return many_rows(q) ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS, 1, 0, 1, true>(
+        return many_rows(q) ? launch_ring<kRms, 2, 8, 12, 1, 2, false, CS, 1, 0, 1, true, 1>(
                                   q, s, cta_status, cta_capacity)
-                            : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS, 0, 0, 1, true>(
+                            : launch_ring<kRms, 2, 8, 8, 1, 2, false, CS, 0, 0, 1, true, 1>(
                                   q, s, cta_status, cta_capacity);
     case 6144:
         return launch_ring<kRms, 3, 8, 12, 3, 2, false, CS, 0, 0, 1, true>(q, s, cta_status, cta_capacity);
