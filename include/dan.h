@@ -45,6 +45,11 @@
  *    pointers are DEVICE pointers owned by the caller; the library never
  *    allocates, frees or synchronises.  `stream` is a cudaStream_t (NULL =
  *    the legacy default stream); the launch is asynchronous on it.
+ *  - Launches allow programmatic dependent launch: a kernel may begin while
+ *    the previous kernel in the stream is finishing.  Until that kernel has
+ *    completed it only sets up its shared memory and hints its first inputs
+ *    into L2 (a hint returns no data); it reads inputs only after waiting
+ *    for that completion, so stream order holds exactly.
  *  - Row tensors [B, T, D] are contiguous, row r = b*T + t.  Per-batch
  *    vectors (scale, shift, gate) are rows of a [B, D] matrix whose batch
  *    stride is `vec_bstride` elements (>= D, a multiple of 8), e.g. chunks
